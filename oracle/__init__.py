@@ -1,0 +1,180 @@
+"""Float64 CPU oracle for the attention forward -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg (``bench.py``) may import this package.  The product path
+(``attention_flash_attn_fwd_gb300``) never imports, loads or calls it, and it
+imports nothing from the product.
+
+The arithmetic lives in ``attn_oracle.c`` (plain C, float64, POSIX threads);
+this module compiles it with gcc, widens inputs exactly to float64 and calls
+it through ctypes.  What the oracle computes and which passages it follows
+are stated at the top of ``attn_oracle.c``:
+
+* prefill: ``O = softmax(scale * Q K^T + causal mask) V`` over BHSD or BSHD
+  tensors, bottom-right causal alignment, ``lse = ln sum exp`` per row
+  (Wave February 2025 Release, "Prefill attention kernel"; WAVE MLSys 2026
+  summary, Attention (prefill), Figures 2-4, and Assumption 1 on BHSD/BSHD);
+* decode: one query per head against a sequence's first ``kv_len`` keys read
+  through a page table, grouped-query heads ``g = h // (H_q // H_kv)``
+  (Wave February 2025 Release, FlashDecoding list: paged flash decoding and
+  the fake-page-table test fixture).
+
+Every function here is pinned by ``tests/test_oracle.py`` against library
+routines, closed forms and analytic fixtures; no part is left unpinned.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+
+BHSD = 0
+BSHD = 1
+
+_lib = None
+_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compile ``attn_oracle.c`` into ``oracle/_build/liboracle.so``.
+
+    Plain ``-O2``: no fast-math, no ``-march=native``, so the same source
+    gives the same float64 results on x86_64 and aarch64 hosts.
+    """
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + ".tmp.%d" % os.getpid()
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+           "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            dp = ctypes.POINTER(ctypes.c_double)
+            ip = ctypes.POINTER(ctypes.c_int32)
+            L = ctypes.c_long
+            lib.oracle_prefill_f64.argtypes = [dp, dp, dp, dp, dp, L, L, L, L, L,
+                                               ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_double, ctypes.c_int]
+            lib.oracle_prefill_f64.restype = ctypes.c_int
+            lib.oracle_decode_f64.argtypes = [dp, dp, dp, ip, ip, dp, dp, L, L, L,
+                                              L, L, L, ctypes.c_double, ctypes.c_int]
+            lib.oracle_decode_f64.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def default_threads() -> int:
+    """Threads the oracle uses by default: every core this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover - non-Linux
+        return os.cpu_count() or 1
+
+
+def _f64(x) -> np.ndarray:
+    """Exact widening of a numpy array or torch tensor (any float dtype) to a
+    contiguous float64 numpy array."""
+    if hasattr(x, "detach"):  # torch tensor, possibly fp16/bf16
+        x = x.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _i32(x) -> np.ndarray:
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu").numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.int32))
+
+
+def _dptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _iptr(a):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+
+def prefill(q, k, v, *, causal: bool, scale: float, layout: int = BHSD,
+            n_threads: int | None = None):
+    """Attention forward in float64.
+
+    ``q``: [B,H,S_q,D] (BHSD) or [B,S_q,H,D] (BSHD); ``k``, ``v``: the same
+    layout with S_kv rows.  Returns ``(o, lse)`` as float64 numpy arrays:
+    ``o`` in q's layout, ``lse`` [B,H,S_q] natural-log (``-inf`` for a row
+    with no visible key, whose ``o`` is 0).
+    """
+    q64, k64, v64 = _f64(q), _f64(k), _f64(v)
+    if layout == BHSD:
+        B, H, S_q, D = q64.shape
+        S_kv = k64.shape[2]
+        kv_shape = (B, H, S_kv, D)
+    elif layout == BSHD:
+        B, S_q, H, D = q64.shape
+        S_kv = k64.shape[1]
+        kv_shape = (B, S_kv, H, D)
+    else:
+        raise ValueError("layout must be BHSD (0) or BSHD (1)")
+    if k64.shape != kv_shape or v64.shape != kv_shape:
+        raise ValueError("k and v must be %r, got %r and %r" % (kv_shape, k64.shape, v64.shape))
+    o = np.zeros(q64.shape, dtype=np.float64)
+    lse = np.zeros((B, H, S_q), dtype=np.float64)
+    rc = _load().oracle_prefill_f64(_dptr(q64), _dptr(k64), _dptr(v64), _dptr(o), _dptr(lse),
+                                    B, H, S_q, S_kv, D, int(layout), int(bool(causal)),
+                                    float(scale), int(n_threads or default_threads()))
+    if rc != 0:
+        raise RuntimeError("oracle_prefill_f64 failed (rc=%d)" % rc)
+    return o, lse
+
+
+def decode(q, k_pool, v_pool, kv_lens, *, scale: float, page_table=None,
+           n_threads: int | None = None):
+    """Seq_len=1 attention over a paged (or contiguous) KV cache, float64.
+
+    ``q``: [B,H_q,D].  Paged: ``k_pool``/``v_pool`` [num_pages, page_size,
+    H_kv, D] and ``page_table`` [B, max_pages] int32.  Contiguous
+    (``page_table is None``): ``k_pool``/``v_pool`` [B, S_max, H_kv, D].
+    ``kv_lens``: [B] int32.  Returns ``(o [B,H_q,D], lse [B,H_q])``.
+    """
+    q64, k64, v64 = _f64(q), _f64(k_pool), _f64(v_pool)
+    lens = _i32(kv_lens)
+    B, H_q, D = q64.shape
+    _, page_size, H_kv, D2 = k64.shape
+    if D2 != D or v64.shape != k64.shape:
+        raise ValueError("k_pool/v_pool shape mismatch")
+    if lens.shape != (B,):
+        raise ValueError("kv_lens must be [B]")
+    pt = None
+    max_pages = 1
+    if page_table is not None:
+        pt = _i32(page_table)
+        if pt.ndim != 2 or pt.shape[0] != B:
+            raise ValueError("page_table must be [B, max_pages]")
+        max_pages = pt.shape[1]
+    elif k64.shape[0] != B:
+        raise ValueError("contiguous k/v must be [B, S_max, H_kv, D]")
+    o = np.zeros((B, H_q, D), dtype=np.float64)
+    lse = np.zeros((B, H_q), dtype=np.float64)
+    rc = _load().oracle_decode_f64(_dptr(q64), _dptr(k64), _dptr(v64), _iptr(pt), _iptr(lens),
+                                   _dptr(o), _dptr(lse), B, H_q, H_kv, D, page_size, max_pages,
+                                   float(scale), int(n_threads or default_threads()))
+    if rc != 0:
+        raise RuntimeError("oracle_decode_f64 failed (rc=%d)" % rc)
+    return o, lse

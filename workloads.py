@@ -1,0 +1,226 @@
+"""Seeded synthetic inputs shared by the tests, the smoke check and the benchmark.
+
+This module holds no attention arithmetic: it only draws random tensors and
+lays out KV pages.  Both the CUDA path's tests and the float64 oracle are fed
+from it, so they see bit-identical inputs.
+
+Recipe (every draw uses a CPU ``torch.Generator`` seeded with ``seed``):
+
+* prefill: Q, K, V drawn in that order as float32 ``randn`` in the layout's
+  own shape ([B,H,S,D] for BHSD, [B,S,H,D] for BSHD), multiplied by ``std``
+  (exact for 0.5) and rounded to nearest-even into fp16/bf16.
+* decode: first ``kv_lens`` (``randint`` uniform on [kv_min, kv_max]), then
+  Q [B,H_q,D], then for each sequence b in order its K rows then its V rows
+  ([kv_len_b, H_kv, D], float32 ``randn`` rounded to bf16/fp16), then the page
+  permutation (``randperm`` over the data pages).
+  Contiguous KV is [B, S_max, H_kv, D]; rows at or past ``kv_len_b`` hold the
+  finite poison value 1e4.  Paged KV is a pool of 16-token pages
+  [num_pages, page_size, H_kv, D]: sequence b owns ceil(kv_len_b/page_size)
+  data pages placed by the permutation, one extra poison page (all 1e4) is
+  appended, unused page-table entries point at it, and page tail slots hold
+  1e4 too, so a masking bug is loud but never reads outside the pool.
+
+The five named workloads follow the configurations this library is measured
+on; their shapes mirror the pages' LLM attention workloads (e.g. the
+Llama-2-13B-like 40-head, D=128 shape of the WAVE MLSys 2026 summary,
+Attention (prefill) and Figure 8).  No public suite or dataset is involved.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+POISON = 1.0e4
+
+_DTYPES = {"fp16": torch.float16, "bf16": torch.bfloat16}
+
+
+@dataclass(frozen=True)
+class PrefillCase:
+    name: str
+    B: int
+    H: int
+    S_q: int
+    S_kv: int
+    D: int
+    layout: str  # "bhsd" or "bshd"
+    dtype: str  # "fp16" or "bf16"
+    causal: bool
+    std: float = 1.0
+    seed: int = 0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+    def flops(self) -> float:
+        """Algorithmic FLOPs: 4*D per visible (query, key) pair (QK^T and PV)."""
+        return 4.0 * self.B * self.H * self.D * visible_pairs(self.S_q, self.S_kv, self.causal)
+
+    def bytes(self) -> int:
+        el = 2
+        return el * self.B * self.H * self.D * (2 * self.S_q + 2 * self.S_kv)
+
+
+@dataclass(frozen=True)
+class DecodeCase:
+    name: str
+    B: int
+    H_q: int
+    H_kv: int
+    D: int
+    kv_min: int
+    kv_max: int
+    S_max: int
+    paged: bool
+    page_size: int = 16
+    dtype: str = "bf16"
+    seed: int = 0
+    num_splits: int = 0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+    @property
+    def max_pages(self) -> int:
+        return -(-self.S_max // self.page_size)
+
+
+def visible_pairs(S_q: int, S_kv: int, causal: bool) -> int:
+    """Number of (query, key) pairs the mask leaves visible (bottom-right causal)."""
+    if not causal:
+        return S_q * S_kv
+    off = S_kv - S_q
+    total = 0
+    # row i sees keys 0 .. min(S_kv-1, i+off)
+    for i in range(S_q):
+        total += max(0, min(S_kv, i + off + 1))
+    return total
+
+
+# The five workloads (tiny oracle case, two prefill shapes, two decode shapes).
+C1 = PrefillCase("prefill_tiny_bhsd_fp16", 1, 2, 128, 128, 64, "bhsd", "fp16", False)
+C2 = PrefillCase("prefill_bhsd_fp16_b4_h32_s4096_d128", 4, 32, 4096, 4096, 128, "bhsd", "fp16", False)
+C2_CAUSAL = PrefillCase("prefill_bhsd_fp16_b4_h32_s4096_d128_causal", 4, 32, 4096, 4096, 128,
+                        "bhsd", "fp16", True)
+C3 = PrefillCase("prefill_bshd_bf16_b8_h40_s2048_d128_causal", 8, 40, 2048, 2048, 128, "bshd",
+                 "bf16", True, std=0.5)
+C4 = DecodeCase("decode_contig_bf16_b32_hq32_hkv8_d128", 32, 32, 8, 128, 1024, 32768, 32768,
+                paged=False)
+C5 = DecodeCase("decode_paged16_bf16_b32_hq32_hkv8_d128", 32, 32, 8, 128, 1, 32768, 32768,
+                paged=True)
+
+
+def _gen(seed: int) -> torch.Generator:
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    return g
+
+
+def _randn(g, shape, std, dtype):
+    x = torch.randn(shape, generator=g, dtype=torch.float32)
+    if std != 1.0:
+        x.mul_(std)
+    return x.to(dtype)
+
+
+def prefill_shape(B, H, S, D, layout):
+    return (B, H, S, D) if layout == "bhsd" else (B, S, H, D)
+
+
+def make_prefill(case: PrefillCase):
+    """Return CPU tensors (q, k, v) for a prefill case."""
+    g = _gen(case.seed)
+    dt = _DTYPES[case.dtype]
+    q = _randn(g, prefill_shape(case.B, case.H, case.S_q, case.D, case.layout), case.std, dt)
+    k = _randn(g, prefill_shape(case.B, case.H, case.S_kv, case.D, case.layout), case.std, dt)
+    v = _randn(g, prefill_shape(case.B, case.H, case.S_kv, case.D, case.layout), case.std, dt)
+    return q, k, v
+
+
+@dataclass
+class DecodeInputs:
+    q: torch.Tensor  # [B, H_q, D]
+    k: torch.Tensor  # contiguous [B, S_max, H_kv, D] or pool [P, page_size, H_kv, D]
+    v: torch.Tensor
+    kv_lens: torch.Tensor  # [B] int32
+    page_table: torch.Tensor | None = None  # [B, max_pages] int32
+    page_size: int = 0
+    max_pages: int = 1
+    extra: dict = field(default_factory=dict)
+
+    def kv_bytes(self) -> int:
+        """Algorithmic K/V bytes one decode pass must read (kv_len rows per (b, kv head))."""
+        H_kv, D = self.k.shape[2], self.k.shape[3]
+        el = self.k.element_size()
+        return int(self.kv_lens.to(torch.int64).sum().item()) * H_kv * D * el * 2
+
+
+def make_decode(case: DecodeCase, kv_lens=None) -> DecodeInputs:
+    """Return CPU tensors for a decode case (see the module docstring recipe)."""
+    g = _gen(case.seed)
+    dt = _DTYPES[case.dtype]
+    if kv_lens is None:
+        kv_lens = torch.randint(case.kv_min, case.kv_max + 1, (case.B,), generator=g,
+                                dtype=torch.int64)
+    kv_lens = torch.as_tensor(kv_lens, dtype=torch.int64)
+    assert int(kv_lens.max()) <= case.S_max and int(kv_lens.min()) >= 0
+    q = _randn(g, (case.B, case.H_q, case.D), 1.0, dt)
+    rows_k, rows_v = [], []
+    for b in range(case.B):
+        n = int(kv_lens[b])
+        rows_k.append(_randn(g, (n, case.H_kv, case.D), 1.0, dt))
+        rows_v.append(_randn(g, (n, case.H_kv, case.D), 1.0, dt))
+    lens32 = kv_lens.to(torch.int32)
+    if not case.paged:
+        k = torch.full((case.B, case.S_max, case.H_kv, case.D), POISON, dtype=dt)
+        v = torch.full((case.B, case.S_max, case.H_kv, case.D), POISON, dtype=dt)
+        for b in range(case.B):
+            n = int(kv_lens[b])
+            k[b, :n] = rows_k[b]
+            v[b, :n] = rows_v[b]
+        return DecodeInputs(q, k, v, lens32, None, case.S_max, 1)
+    ps = case.page_size
+    pages_per_seq = [-(-int(n) // ps) for n in kv_lens.tolist()]
+    n_data = sum(pages_per_seq)
+    perm = torch.randperm(n_data, generator=g)
+    poison_page = n_data
+    k = torch.full((n_data + 1, ps, case.H_kv, case.D), POISON, dtype=dt)
+    v = torch.full((n_data + 1, ps, case.H_kv, case.D), POISON, dtype=dt)
+    page_table = torch.full((case.B, case.max_pages), poison_page, dtype=torch.int32)
+    cursor = 0
+    for b in range(case.B):
+        n = int(kv_lens[b])
+        for p in range(pages_per_seq[b]):
+            phys = int(perm[cursor])
+            cursor += 1
+            page_table[b, p] = phys
+            lo, hi = p * ps, min(n, (p + 1) * ps)
+            k[phys, : hi - lo] = rows_k[b][lo:hi]
+            v[phys, : hi - lo] = rows_v[b][lo:hi]
+    return DecodeInputs(q, k, v, lens32, page_table, ps, case.max_pages)
+
+
+def contiguous_view_of(inp: DecodeInputs, S_max: int | None = None) -> DecodeInputs:
+    """Re-lay a paged DecodeInputs as contiguous [B, S_max, H_kv, D] (poison past kv_len).
+
+    Pure data movement: used by tests that check paged == contiguous."""
+    if inp.page_table is None:
+        return inp
+    B = inp.q.shape[0]
+    ps = inp.page_size
+    S_max = S_max or inp.max_pages * ps
+    H_kv, D = inp.k.shape[2], inp.k.shape[3]
+    k = torch.full((B, S_max, H_kv, D), POISON, dtype=inp.k.dtype)
+    v = torch.full((B, S_max, H_kv, D), POISON, dtype=inp.v.dtype)
+    for b in range(B):
+        n = int(inp.kv_lens[b])
+        for p in range(-(-n // ps)):
+            lo, hi = p * ps, min(n, (p + 1) * ps)
+            phys = int(inp.page_table[b, p])
+            k[b, lo:hi] = inp.k[phys, : hi - lo]
+            v[b, lo:hi] = inp.v[phys, : hi - lo]
+    return DecodeInputs(inp.q, k, v, inp.kv_lens, None, S_max, 1)
