@@ -1,0 +1,253 @@
+"""GB300 (sm_103a) fused attention forward: Python binding of ``libattn_gb300.so``.
+
+The binding only marshals arguments: every step of the computation runs in the
+library's CUDA kernels.  There is no CPU or PyTorch fallback; if the library
+cannot be built or loaded, importing the functions below raises.
+
+Two layers:
+
+* ``attn_prefill_fwd`` / ``attn_decode_fwd`` -- the C entry points of
+  ``include/attn_gb300.h`` with the same names and arguments (raw device
+  pointers as ints, ``stream`` as a ``cudaStream_t`` handle int).
+* ``prefill`` / ``decode`` -- convenience wrappers over torch CUDA tensors
+  (torch is used for device memory and the current stream only).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+from . import _build
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = -1
+ATTN_ERR_UNSUPPORTED = -2
+ATTN_ERR_CUDA = -3
+ATTN_ERR_NO_MEMORY = -4
+ATTN_ERR_DEVICE_TIMEOUT = -5
+
+ATTN_BHSD = 0
+ATTN_BSHD = 1
+ATTN_F16 = 0
+ATTN_BF16 = 1
+
+_STATUS_NAMES = {
+    ATTN_OK: "ATTN_OK",
+    ATTN_ERR_INVALID_ARG: "ATTN_ERR_INVALID_ARG",
+    ATTN_ERR_UNSUPPORTED: "ATTN_ERR_UNSUPPORTED",
+    ATTN_ERR_CUDA: "ATTN_ERR_CUDA",
+    ATTN_ERR_NO_MEMORY: "ATTN_ERR_NO_MEMORY",
+    ATTN_ERR_DEVICE_TIMEOUT: "ATTN_ERR_DEVICE_TIMEOUT",
+}
+
+# Names the header exports (checked against include/attn_gb300.h by the tests).
+EXPORTED = ("attn_prefill_fwd", "attn_decode_fwd", "attn_last_error", "attn_device_error",
+            "attn_set_wait_limit_ns", "attn_release_workspace", "attn_version")
+
+
+class AttnError(RuntimeError):
+    """A library call returned a non-OK status."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__("%s: %s" % (_STATUS_NAMES.get(status, str(status)), message))
+        self.status = status
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """Load (building first if needed) the shared library and declare its ABI."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            L = ctypes.CDLL(path)
+            vp, i32p = ctypes.c_void_p, ctypes.c_void_p
+            ci, cf = ctypes.c_int, ctypes.c_float
+            L.attn_prefill_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, cf,
+                                           vp]
+            L.attn_prefill_fwd.restype = ci
+            L.attn_decode_fwd.argtypes = [vp, vp, vp, i32p, i32p, vp, ci, ci, ci, ci, ci, ci, ci,
+                                          ci, cf, ci, vp]
+            L.attn_decode_fwd.restype = ci
+            L.attn_last_error.argtypes = []
+            L.attn_last_error.restype = ctypes.c_char_p
+            L.attn_device_error.argtypes = [ctypes.POINTER(ctypes.c_int), ci]
+            L.attn_device_error.restype = ci
+            L.attn_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+            L.attn_set_wait_limit_ns.restype = None
+            L.attn_release_workspace.argtypes = []
+            L.attn_release_workspace.restype = ci
+            L.attn_version.argtypes = []
+            L.attn_version.restype = ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+def last_error() -> str:
+    return lib().attn_last_error().decode()
+
+
+def _check(status: int) -> int:
+    if status != ATTN_OK:
+        raise AttnError(status, last_error())
+    return status
+
+
+# --------------------------------------------------------------- raw C ABI
+
+
+def attn_prefill_fwd(q, k, v, o, lse, B, H, S_q, S_kv, D, layout, dtype, causal, scale,
+                     stream) -> int:
+    """C ``attn_prefill_fwd``; pointers and stream as ints.  Returns the status."""
+    return lib().attn_prefill_fwd(q, k, v, o, lse, B, H, S_q, S_kv, D, layout, dtype, causal,
+                                  scale, stream)
+
+
+def attn_decode_fwd(q, k_pool, v_pool, page_table, kv_lens, o, B, H_q, H_kv, D, page_size,
+                    max_pages_per_seq, num_pages, num_splits, scale, dtype, stream) -> int:
+    """C ``attn_decode_fwd``; pointers and stream as ints.  Returns the status."""
+    return lib().attn_decode_fwd(q, k_pool, v_pool, page_table, kv_lens, o, B, H_q, H_kv, D,
+                                 page_size, max_pages_per_seq, num_pages, num_splits, scale,
+                                 dtype, stream)
+
+
+def attn_last_error() -> str:
+    return last_error()
+
+
+def attn_device_error(clear: bool = True) -> int:
+    """Synchronize, then return (and clear) the device error word; 0 means none."""
+    w = ctypes.c_int(0)
+    lib().attn_device_error(ctypes.byref(w), 1 if clear else 0)
+    return w.value
+
+
+def attn_set_wait_limit_ns(ns: int) -> None:
+    lib().attn_set_wait_limit_ns(ns)
+
+
+def attn_release_workspace() -> int:
+    return lib().attn_release_workspace()
+
+
+def attn_version() -> str:
+    return lib().attn_version().decode()
+
+
+# ---------------------------------------------------------- torch wrappers
+
+
+def _torch():
+    import torch  # noqa: PLC0415 - torch is only the memory/stream provider
+
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float16:
+        return ATTN_F16
+    if t.dtype == torch.bfloat16:
+        return ATTN_BF16
+    raise TypeError("attention tensors must be float16 or bfloat16, got %s" % t.dtype)
+
+
+def _require_cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def _stream_handle(stream) -> int:
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def prefill(q, k, v, *, causal: bool = False, scale: float | None = None,
+            layout: str = "bhsd", out=None, lse=None, return_lse: bool = False, stream=None):
+    """Attention forward over torch CUDA tensors.
+
+    ``layout="bhsd"``: q [B,H,S_q,D], k/v [B,H,S_kv,D]; ``"bshd"``: q [B,S_q,H,D],
+    k/v [B,S_kv,H,D].  Returns ``o`` (and ``lse`` [B,H,S_q] fp32 if requested).
+    """
+    torch = _torch()
+    _require_cuda(q, k, v, out, lse)
+    if layout == "bhsd":
+        B, H, S_q, D = q.shape
+        S_kv = k.shape[2]
+        code = ATTN_BHSD
+    elif layout == "bshd":
+        B, S_q, H, D = q.shape
+        S_kv = k.shape[1]
+        code = ATTN_BSHD
+    else:
+        raise ValueError("layout must be 'bhsd' or 'bshd'")
+    if k.shape != v.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("k and v must match each other and q's dtype")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if return_lse and lse is None:
+        lse = torch.empty((B, H, S_q), device=q.device, dtype=torch.float32)
+    _check(attn_prefill_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                            lse.data_ptr() if lse is not None else None, B, H, S_q, S_kv, D,
+                            code, _dtype_code(q), int(bool(causal)), float(scale),
+                            _stream_handle(stream)))
+    return (out, lse) if return_lse else out
+
+
+def decode(q, k_pool, v_pool, kv_lens, *, page_table=None, num_pages: int | None = None,
+           num_splits: int = 0, scale: float | None = None, out=None, stream=None):
+    """Decode attention over torch CUDA tensors.
+
+    ``q`` [B,H_q,D]; paged: ``k_pool``/``v_pool`` [num_pages, page_size, H_kv, D] and
+    ``page_table`` [B, max_pages] int32; contiguous (``page_table=None``):
+    ``k_pool``/``v_pool`` [B, S_max, H_kv, D].  ``kv_lens`` [B] int32 (CUDA).
+    """
+    torch = _torch()
+    _require_cuda(q, k_pool, v_pool, kv_lens, page_table, out)
+    B, H_q, D = q.shape
+    n_pages, page_size, H_kv, D2 = k_pool.shape
+    if D2 != D or v_pool.shape != k_pool.shape:
+        raise ValueError("k_pool/v_pool must be [pages, page_size, H_kv, D]")
+    if kv_lens.dtype != torch.int32 or (page_table is not None and page_table.dtype != torch.int32):
+        raise TypeError("kv_lens and page_table must be int32")
+    if page_table is not None:
+        max_pages = page_table.shape[1]
+        num_pages = n_pages if num_pages is None else num_pages
+    else:
+        max_pages = 1
+        num_pages = B
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    _check(attn_decode_fwd(q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(),
+                           page_table.data_ptr() if page_table is not None else None,
+                           kv_lens.data_ptr(), out.data_ptr(), B, H_q, H_kv, D, page_size,
+                           max_pages, num_pages, int(num_splits), float(scale), _dtype_code(q),
+                           _stream_handle(stream)))
+    return out
+
+
+def check_device_error() -> None:
+    """Raise AttnError if any kernel recorded a device error (synchronizes)."""
+    w = ctypes.c_int(0)
+    st = lib().attn_device_error(ctypes.byref(w), 1)
+    if st != ATTN_OK:
+        raise AttnError(st, last_error())
+
+
+__all__ = [n for n in dir() if n.startswith(("attn_", "ATTN_"))] + [
+    "AttnError", "prefill", "decode", "lib", "library_path", "check_device_error", "EXPORTED"]

@@ -1,0 +1,353 @@
+// attn_api.cu -- the C ABI (include/attn_gb300.h): argument validation, TMA
+// tensor-map encoding, the decode split plan and workspace, error reporting.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <mutex>
+#include <string>
+
+#include "../../include/attn_gb300.h"
+#include "decode_sm103a.h"
+#include "prefill_sm103a.h"
+#include "tmap.h"
+
+namespace {
+
+constexpr uint64_t kDefaultWaitLimitNs = 4000000000ull;  // 4 s
+constexpr int kMaxDevices = 64;
+
+thread_local std::string t_last_error;
+std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitLimitNs};
+
+__device__ int g_device_error_word = 0;
+
+attn_status fail(attn_status s, const std::string& msg) {
+  t_last_error = msg;
+  return s;
+}
+
+attn_status fail_cuda(cudaError_t e, const char* what) {
+  return fail(ATTN_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+struct DeviceState {
+  std::mutex mu;
+  int* err_word = nullptr;    // device address of g_device_error_word
+  int num_sms = 0;
+  void* workspace = nullptr;  // decode split partials
+  size_t workspace_bytes = 0;
+};
+
+DeviceState g_dev[kMaxDevices];
+
+// Per-device set-up, done once with the device current.
+attn_status device_state(DeviceState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(ATTN_ERR_UNSUPPORTED, "device index too large");
+  DeviceState& st = g_dev[dev];
+  std::lock_guard<std::mutex> lk(st.mu);
+  if (st.err_word == nullptr) {
+    e = cudaGetSymbolAddress(reinterpret_cast<void**>(&st.err_word), g_device_error_word);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaGetSymbolAddress(error word)");
+    e = cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute(SM count)");
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3) {
+      st.err_word = nullptr;
+      return fail(ATTN_ERR_UNSUPPORTED, "this library is built for sm_103a (GB300) only; device is sm_" +
+                                            std::to_string(major) + std::to_string(minor));
+    }
+  }
+  *out = &st;
+  return ATTN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Prefill tensor map over a [B,H,S,D] (BHSD) or [B,S,H,D] (BSHD) tensor.
+// BHSD dims (D, S, H, B); BSHD dims (D, H, S, B) so strides grow outward.
+bool prefill_map(CUtensorMap* m, const void* base, int B, int H, int S, int D, bool bshd,
+                 bool bf16) {
+  const uint64_t el = 2;
+  uint64_t dims[4], strides[3];
+  uint32_t box[4];
+  if (!bshd) {
+    dims[0] = D; dims[1] = S; dims[2] = H; dims[3] = B;
+    strides[0] = el * D; strides[1] = el * D * S; strides[2] = el * D * S * H;
+    box[0] = 64; box[1] = attn_sm103a::prefill_box_rows(); box[2] = 1; box[3] = 1;
+  } else {
+    dims[0] = D; dims[1] = H; dims[2] = S; dims[3] = B;
+    strides[0] = el * D; strides[1] = el * D * H; strides[2] = el * D * H * S;
+    box[0] = 64; box[1] = 1; box[2] = attn_sm103a::prefill_box_rows(); box[3] = 1;
+  }
+  return attn_host::encode_tiled_16bit(m, base, 4, dims, strides, box, bf16,
+                                       CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Decode tensor map over a pool [num_pages, page_size, H_kv, D]: dims
+// (D, H_kv, page_size, num_pages), box (64, 1, rows, 1).
+bool decode_map(CUtensorMap* m, const void* base, int num_pages, int page_size, int H_kv, int D,
+                int box_rows, bool bf16) {
+  const uint64_t el = 2;
+  uint64_t dims[4] = {static_cast<uint64_t>(D), static_cast<uint64_t>(H_kv),
+                      static_cast<uint64_t>(page_size), static_cast<uint64_t>(num_pages)};
+  uint64_t strides[3] = {el * D, el * D * H_kv, el * D * H_kv * page_size};
+  uint32_t box[4] = {64, 1, static_cast<uint32_t>(box_rows), 1};
+  return attn_host::encode_tiled_16bit(m, base, 4, dims, strides, box, bf16,
+                                       CU_TENSOR_MAP_SWIZZLE_128B,
+                                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+}
+
+int env_int(const char* name, int dflt) {
+  const char* v = std::getenv(name);
+  if (!v || !*v) return dflt;
+  return std::atoi(v);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* attn_version(void) { return "attn_gb300 0.1.0 (sm_103a)"; }
+
+const char* attn_last_error(void) { return t_last_error.c_str(); }
+
+void attn_set_wait_limit_ns(uint64_t ns) {
+  g_wait_limit_ns.store(ns ? ns : kDefaultWaitLimitNs);
+}
+
+attn_status attn_device_error(int* word, int clear) {
+  DeviceState* st = nullptr;
+  attn_status s = device_state(&st);
+  if (s != ATTN_OK) return s;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceSynchronize");
+  int w = 0;
+  e = cudaMemcpy(&w, st->err_word, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail_cuda(e, "read device error word");
+  if (clear && w != 0) {
+    int zero = 0;
+    e = cudaMemcpy(st->err_word, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return fail_cuda(e, "clear device error word");
+  }
+  if (word) *word = w;
+  if (w != 0) {
+    char buf[96];
+    std::snprintf(buf, sizeof(buf), "device error word 0x%08x (code %d, site %d)", w, w >> 16,
+                  w & 0xFFFF);
+    return fail(ATTN_ERR_DEVICE_TIMEOUT, buf);
+  }
+  return ATTN_OK;
+}
+
+attn_status attn_prefill_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int B, int H, int S_q, int S_kv, int D, attn_layout layout,
+                             attn_dtype dtype, int causal, float scale, cudaStream_t stream) {
+  if (B < 0 || H < 0 || S_q < 0 || S_kv < 0)
+    return fail(ATTN_ERR_INVALID_ARG, "B, H, S_q and S_kv must be >= 0");
+  if (layout != ATTN_BHSD && layout != ATTN_BSHD)
+    return fail(ATTN_ERR_INVALID_ARG, "layout must be ATTN_BHSD or ATTN_BSHD");
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16)
+    return fail(ATTN_ERR_INVALID_ARG, "dtype must be ATTN_F16 or ATTN_BF16");
+  if (causal != 0 && causal != 1) return fail(ATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (!(std::isfinite(scale) && scale > 0.f))
+    return fail(ATTN_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (D != 64 && D != 128) return fail(ATTN_ERR_UNSUPPORTED, "D must be 64 or 128");
+  if (static_cast<int64_t>(B) * H * S_q == 0) return ATTN_OK;  // nothing to compute
+  if (!q || !o || (S_kv > 0 && (!k || !v)))
+    return fail(ATTN_ERR_INVALID_ARG, "q, k, v and o must be non-NULL");
+  if (!aligned16(q) || !aligned16(o) || (S_kv > 0 && (!aligned16(k) || !aligned16(v))))
+    return fail(ATTN_ERR_INVALID_ARG, "q, k, v and o must be 16-byte aligned");
+  const int64_t elems = static_cast<int64_t>(B) * H * (S_q > S_kv ? S_q : S_kv) * D;
+  if (elems * 2 >= (int64_t(1) << 40))
+    return fail(ATTN_ERR_UNSUPPORTED, "tensor too large for one TMA descriptor");
+  const int rows = attn_sm103a::prefill_rows_per_cta();
+  const int64_t n_qb = (S_q + rows - 1) / rows;
+  if (static_cast<int64_t>(B) * H * n_qb > 0x7FFFFFFF)
+    return fail(ATTN_ERR_UNSUPPORTED, "grid too large");
+
+  DeviceState* st = nullptr;
+  attn_status s = device_state(&st);
+  if (s != ATTN_OK) return s;
+
+  const bool bshd = layout == ATTN_BSHD;
+  const bool bf16 = dtype == ATTN_BF16;
+  CUtensorMap mq, mk, mv, mo;
+  // With S_kv == 0 no K/V tile is ever loaded; q stands in as a valid base.
+  const int S_kv_map = S_kv > 0 ? S_kv : 1;
+  const void* kb = S_kv > 0 ? k : q;
+  const void* vb = S_kv > 0 ? v : q;
+  if (!prefill_map(&mq, q, B, H, S_q, D, bshd, bf16) ||
+      !prefill_map(&mk, kb, B, H, S_kv_map, D, bshd, bf16) ||
+      !prefill_map(&mv, vb, B, H, S_kv_map, D, bshd, bf16) ||
+      !prefill_map(&mo, o, B, H, S_q, D, bshd, bf16))
+    return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed for a prefill tensor");
+
+  attn_sm103a::PrefillParams p{};
+  p.lse = lse;
+  p.B = B;
+  p.H = H;
+  p.S_q = S_q;
+  p.S_kv = S_kv;
+  p.num_q_blocks = static_cast<int>(n_qb);
+  p.causal = causal;
+  p.bshd = bshd ? 1 : 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.err = st->err_word;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  cudaError_t e = attn_sm103a::prefill_launch(mq, mk, mv, mo, p, D, bf16, stream);
+  if (e != cudaSuccess) return fail_cuda(e, "prefill launch");
+  return ATTN_OK;
+}
+
+attn_status attn_decode_fwd(const void* q, const void* k_pool, const void* v_pool,
+                            const int32_t* page_table, const int32_t* kv_lens, void* o, int B,
+                            int H_q, int H_kv, int D, int page_size, int max_pages_per_seq,
+                            int num_pages, int num_splits, float scale, attn_dtype dtype,
+                            cudaStream_t stream) {
+  if (B < 0) return fail(ATTN_ERR_INVALID_ARG, "B must be >= 0");
+  if (H_q <= 0 || H_kv <= 0) return fail(ATTN_ERR_INVALID_ARG, "H_q and H_kv must be > 0");
+  if (H_q % H_kv != 0) return fail(ATTN_ERR_INVALID_ARG, "H_q must be a multiple of H_kv");
+  if (H_q / H_kv > 16) return fail(ATTN_ERR_UNSUPPORTED, "H_q / H_kv must be <= 16");
+  if (D != 64 && D != 128) return fail(ATTN_ERR_UNSUPPORTED, "D must be 64 or 128");
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16)
+    return fail(ATTN_ERR_INVALID_ARG, "dtype must be ATTN_F16 or ATTN_BF16");
+  if (!(std::isfinite(scale) && scale > 0.f))
+    return fail(ATTN_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (num_splits < 0) return fail(ATTN_ERR_INVALID_ARG, "num_splits must be >= 0");
+  if (page_size <= 0) return fail(ATTN_ERR_INVALID_ARG, "page_size must be > 0");
+  const bool paged = page_table != nullptr;
+  if (paged) {
+    if (max_pages_per_seq <= 0 || num_pages <= 0)
+      return fail(ATTN_ERR_INVALID_ARG, "max_pages_per_seq and num_pages must be > 0");
+    const bool small_ok = page_size <= 64 && 64 % page_size == 0 && page_size >= 8;
+    if (!small_ok && page_size % 64 != 0)
+      return fail(ATTN_ERR_UNSUPPORTED, "page_size must be 8, 16, 32 or a multiple of 64");
+  } else {
+    max_pages_per_seq = 1;
+    if (num_pages != B)
+      return fail(ATTN_ERR_INVALID_ARG, "contiguous cache: num_pages must equal B");
+  }
+  if (B == 0) return ATTN_OK;
+  if (!q || !k_pool || !v_pool || !kv_lens || !o)
+    return fail(ATTN_ERR_INVALID_ARG, "q, k_pool, v_pool, kv_lens and o must be non-NULL");
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(o))
+    return fail(ATTN_ERR_INVALID_ARG, "q, k_pool, v_pool and o must be 16-byte aligned");
+  const int64_t cap = static_cast<int64_t>(max_pages_per_seq) * page_size;
+  if (cap > 0x7FFFFFFF) return fail(ATTN_ERR_UNSUPPORTED, "KV capacity exceeds 2^31 keys");
+  if (static_cast<int64_t>(num_pages) * page_size * H_kv * D * 2 >= (int64_t(1) << 40))
+    return fail(ATTN_ERR_UNSUPPORTED, "KV pool too large for one TMA descriptor");
+
+  DeviceState* st = nullptr;
+  attn_status s = device_state(&st);
+  if (s != ATTN_OK) return s;
+
+  // Split plan.  num_splits > 0 splits every sequence into that many parts;
+  // 0 fixes a chunk length so that the expected work (sequences assumed half
+  // full on average) spans several waves of resident CTAs.
+  const int kt = attn_sm103a::decode_keys_per_tile();
+  int fixed_chunk = 0, max_splits = 0;
+  if (num_splits > 0) {
+    max_splits = num_splits;
+  } else {
+    int chunk = env_int("ATTN_DECODE_SPLIT_CHUNK", 0);
+    if (chunk <= 0) {
+      const double est_keys = static_cast<double>(B) * H_kv * (static_cast<double>(cap) / 2.0);
+      const double target_ctas = 8.0 * 2.0 * st->num_sms;
+      chunk = static_cast<int>(est_keys / target_ctas);
+      if (chunk < 256) chunk = 256;
+      if (chunk > 8192) chunk = 8192;
+    }
+    chunk = (chunk + kt - 1) / kt * kt;
+    fixed_chunk = chunk;
+    max_splits = static_cast<int>((cap + chunk - 1) / chunk);
+    if (max_splits < 1) max_splits = 1;
+  }
+  if (static_cast<int64_t>(max_splits) > 65535)
+    return fail(ATTN_ERR_UNSUPPORTED, "too many splits for one launch");
+
+  // Workspace: o_part [B, H_q, max_splits, D] + lse_part [B, H_q, max_splits].
+  const size_t rows_ws = static_cast<size_t>(B) * H_q * max_splits;
+  const size_t need = rows_ws * D * sizeof(float) + rows_ws * sizeof(float);
+  {
+    std::lock_guard<std::mutex> lk(st->mu);
+    if (st->workspace_bytes < need) {
+      cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+      cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+      if (e != cudaSuccess) return fail_cuda(e, "cudaStreamIsCapturing");
+      if (cs != cudaStreamCaptureStatusNone)
+        return fail(ATTN_ERR_NO_MEMORY,
+                    "decode workspace must grow but the stream is capturing; call once before "
+                    "capture with the largest shapes");
+      if (st->workspace) {
+        cudaDeviceSynchronize();
+        cudaFree(st->workspace);
+        st->workspace = nullptr;
+        st->workspace_bytes = 0;
+      }
+      void* ws = nullptr;
+      e = cudaMalloc(&ws, need);
+      if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(ATTN_ERR_NO_MEMORY, std::string("workspace cudaMalloc: ") + cudaGetErrorString(e));
+      }
+      st->workspace = ws;
+      st->workspace_bytes = need;
+    }
+  }
+
+  const bool bf16 = dtype == ATTN_BF16;
+  const int box_rows = paged ? (page_size < kt ? page_size : kt) : kt;
+  CUtensorMap mk, mv;
+  if (!decode_map(&mk, k_pool, paged ? num_pages : B, page_size, H_kv, D, box_rows, bf16) ||
+      !decode_map(&mv, v_pool, paged ? num_pages : B, page_size, H_kv, D, box_rows, bf16))
+    return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed for the KV pool");
+
+  attn_sm103a::DecodeParams p{};
+  p.q = q;
+  p.page_table = page_table;
+  p.kv_lens = kv_lens;
+  p.o_part = static_cast<float*>(st->workspace);
+  p.lse_part = p.o_part + rows_ws * D;
+  p.B = B;
+  p.H_q = H_q;
+  p.group = H_q / H_kv;
+  p.page_size = page_size;
+  p.max_pages = max_pages_per_seq;
+  p.num_pages = paged ? num_pages : B;
+  p.max_splits = max_splits;
+  p.fixed_chunk = fixed_chunk;
+  p.num_splits = num_splits > 0 ? num_splits : 1;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.err = st->err_word;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  cudaError_t e = attn_sm103a::decode_launch(mk, mv, p, o, D, bf16, stream);
+  if (e != cudaSuccess) return fail_cuda(e, "decode launch");
+  return ATTN_OK;
+}
+
+attn_status attn_release_workspace(void) {
+  DeviceState* st = nullptr;
+  attn_status s = device_state(&st);
+  if (s != ATTN_OK) return s;
+  std::lock_guard<std::mutex> lk(st->mu);
+  if (st->workspace) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceSynchronize");
+    cudaFree(st->workspace);
+    st->workspace = nullptr;
+    st->workspace_bytes = 0;
+  }
+  return ATTN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,31 @@
+// prefill_sm103a.h -- launch interface of the prefill attention kernel.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace attn_sm103a {
+
+struct PrefillParams {
+  float* lse;             // [B, H, S_q] natural-log row sums, or nullptr
+  int B, H, S_q, S_kv;
+  int num_q_blocks;       // ceil(S_q / prefill_rows_per_cta())
+  int causal;             // bottom-right aligned causal mask
+  int bshd;               // 1: tensor maps are (D, H, S, B); 0: (D, S, H, B)
+  float scale_log2;       // softmax scale * log2(e)
+  int* err;               // device error word
+  uint64_t wait_limit_ns; // bound on every mbarrier wait
+};
+
+// Tensor maps: 16-bit elements, 128-byte swizzle, box = 64 columns x
+// prefill_box_rows() rows of one (batch, head).
+cudaError_t prefill_launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                           const CUtensorMap& o, const PrefillParams& p, int D, bool bf16,
+                           cudaStream_t stream);
+
+int prefill_rows_per_cta();
+int prefill_box_rows();
+
+}  // namespace attn_sm103a

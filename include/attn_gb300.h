@@ -1,0 +1,152 @@
+/*
+ * attn_gb300.h -- C ABI of the GB300 (sm_103a) fused attention forward library.
+ *
+ * The library computes the scaled-dot-product attention forward
+ *
+ *     O = softmax(scale * Q K^T + causal mask) V
+ *
+ * in two forms:
+ *   - prefill, over BHSD or BSHD tensors ("Prefill attention kernel" in the
+ *     Wave February 2025 Release, FlashDecoding list; WAVE MLSys 2026 summary,
+ *     Attention (prefill), Figures 2-4, and its Assumption 1: BSHD only swaps
+ *     the boundary indexing of BHSD);
+ *   - seq_len = 1 flash decoding with split KV over a paged or contiguous KV
+ *     cache ("Flash Decoding Kernel with paged attention" and "... without
+ *     paged attention ... with Dynamic Dims", Wave February 2025 Release,
+ *     FlashDecoding list), grouped-query heads, and a log-sum-exp combine of
+ *     the splits (the split-KV grid and its empty-window handling follow the
+ *     ideas of aiter PR 7412, Summary and Changes/Host side).
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller, dense
+ *     (contiguous) in the layout named below, 16-byte aligned.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; 0 is the
+ *     legacy default stream).  No entry point synchronizes the device.
+ *   - Arguments are validated on the host before anything is launched; a bad
+ *     argument returns ATTN_ERR_INVALID_ARG or ATTN_ERR_UNSUPPORTED and
+ *     launches nothing.  attn_last_error() then describes the problem.
+ *   - A launch failure returns ATTN_ERR_CUDA.
+ *   - Kernels never spin without bound: every internal wait has a time limit
+ *     after which the kernel records a device error word and exits;
+ *     attn_device_error() reads it.
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = -1,    /* a pointer, size or layout is invalid */
+  ATTN_ERR_UNSUPPORTED = -2,    /* valid but not implemented (e.g. D not 64/128) */
+  ATTN_ERR_CUDA = -3,           /* a CUDA runtime/driver call failed */
+  ATTN_ERR_NO_MEMORY = -4,      /* workspace could not be (re)allocated */
+  ATTN_ERR_DEVICE_TIMEOUT = -5  /* a kernel wait ran past its time limit */
+} attn_status;
+
+typedef enum { ATTN_BHSD = 0, ATTN_BSHD = 1 } attn_layout;
+
+typedef enum { ATTN_F16 = 0, ATTN_BF16 = 1 } attn_dtype;
+
+/*
+ * Prefill attention forward.
+ *
+ * Defines: O[b,h,i,:] = sum_j softmax_j(scale * q_i . k_j) v_j over the keys j
+ * visible to query i (WAVE MLSys 2026 summary, Attention (prefill)).
+ *
+ *   q   [B,H,S_q,D]  (layout ATTN_BHSD) or [B,S_q,H,D] (ATTN_BSHD), dtype
+ *   k,v [B,H,S_kv,D] or [B,S_kv,H,D], same layout and dtype as q
+ *   o   output, same shape, layout and dtype as q
+ *   lse output [B,H,S_q] fp32, natural-log row sums ln sum_j exp(scale q.k_j);
+ *       may be NULL.  A row with no visible key gets o = 0 and lse = -inf.
+ *   causal  0 or 1.  Causal masking is bottom-right aligned: key j is visible
+ *       to query i iff j <= i + (S_kv - S_q).
+ *   scale   softmax scale, finite and > 0 (typically 1/sqrt(D)).
+ *   D       64 or 128 (else ATTN_ERR_UNSUPPORTED).
+ *   B, H, S_q, S_kv >= 0; B*H*S_q == 0 is a no-op.
+ * Accumulation is fp32; P is rounded to the input dtype before P V; O is
+ * rounded once, to nearest even.
+ */
+ATTN_API attn_status attn_prefill_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int B, int H, int S_q, int S_kv, int D, attn_layout layout,
+                             attn_dtype dtype, int causal, float scale, cudaStream_t stream);
+
+/*
+ * Decode attention forward (one query per head, split KV, paged or contiguous
+ * KV cache).
+ *
+ * Defines: O[b,h,:] = sum_t softmax_t(scale * q[b,h] . k_t) v_t over the keys
+ * t < kv_lens[b] of sequence b, read from kv head g = h / (H_q / H_kv)
+ * (flash decoding, Wave February 2025 Release, FlashDecoding list).
+ *
+ *   q          [B,H_q,D] dtype
+ *   k_pool,    paged: [num_pages, page_size, H_kv, D] dtype;
+ *   v_pool     contiguous (page_table == NULL): [B, page_size, H_kv, D], i.e.
+ *              page_size is the cache capacity S_max and sequence b owns page b
+ *   page_table [B, max_pages_per_seq] int32 pool page ids, or NULL.  Entry
+ *              [b, p] holds logical keys [p*page_size, (p+1)*page_size) of
+ *              sequence b; entries at or past ceil(kv_lens[b]/page_size) are
+ *              never read.  Every entry that is read must be in [0, num_pages).
+ *   kv_lens    [B] int32 on the device, 0 <= kv_lens[b] <= max_pages_per_seq *
+ *              page_size.  A sequence with kv_len 0 gets o = 0.
+ *   o          [B,H_q,D] dtype output.
+ *   page_size  keys per page (multiple of 8, <= 256 when paged).
+ *   max_pages_per_seq  page_table row stride (ADDED to the published
+ *              signature: the table's shape is not otherwise known); 1 when
+ *              contiguous.
+ *   num_pages  number of pages in the pool (ADDED: bounds the gather); B when
+ *              contiguous.
+ *   num_splits 0: split count chosen per sequence from its kv_len on the
+ *              device; > 0: every sequence is split into that many parts.
+ *   scale      softmax scale, finite and > 0.
+ *   dtype      ATTN_F16 or ATTN_BF16 (ADDED: not in the published signature).
+ *   H_q % H_kv == 0, H_q / H_kv <= 16, D == 128 (else ATTN_ERR_UNSUPPORTED).
+ * The library owns a split-partials workspace, grown on demand outside stream
+ * capture; growing it during capture returns ATTN_ERR_NO_MEMORY (call once
+ * with the largest shapes before capturing).
+ */
+ATTN_API attn_status attn_decode_fwd(const void* q, const void* k_pool, const void* v_pool,
+                            const int32_t* page_table, const int32_t* kv_lens, void* o, int B,
+                            int H_q, int H_kv, int D, int page_size, int max_pages_per_seq,
+                            int num_pages, int num_splits, float scale, attn_dtype dtype,
+                            cudaStream_t stream);
+
+/* Message describing the last error returned on the calling thread. */
+ATTN_API const char* attn_last_error(void);
+
+/*
+ * Read (and clear, if `clear` != 0) the device error word of the current
+ * device: 0 when no kernel recorded an error, else (code << 16) | site, where
+ * code 1 = a wait ran past its time limit.  Synchronizes the device first.
+ * Returns ATTN_OK, or ATTN_ERR_DEVICE_TIMEOUT when the word was non-zero.
+ */
+ATTN_API attn_status attn_device_error(int* word, int clear);
+
+/*
+ * Set the time limit (nanoseconds) every kernel wait is bounded by; 0 restores
+ * the default (4 s).  Applies to launches made after the call.
+ */
+ATTN_API void attn_set_wait_limit_ns(uint64_t ns);
+
+/* Free the decode workspace of the current device (not during capture). */
+ATTN_API attn_status attn_release_workspace(void);
+
+/* Library version string. */
+ATTN_API const char* attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

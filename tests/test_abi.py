@@ -1,0 +1,122 @@
+"""The C ABI without a GPU: the library builds and loads, exports every
+function include/attn_gb300.h declares, and rejects bad arguments on the host
+before anything would be launched."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import attention_flash_attn_fwd_gb300 as attn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn_gb300.h")
+
+
+def _declared_functions():
+    with open(HEADER) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"ATTN_API\s+[\w\s\*]+?\b(attn_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_names():
+    assert _declared_functions() == sorted(attn.EXPORTED)
+
+
+def test_library_loads_and_exports_every_declared_symbol():
+    lib = attn.lib()
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", attn.library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT\s+(attn_\w+)", out))
+    assert set(_declared_functions()) <= exported
+    assert attn.attn_version().startswith("attn_gb300")
+
+
+def test_header_compiles_as_plain_c():
+    src = '#include "attn_gb300.h"\nint main(void) { return ATTN_OK; }\n'
+    r = subprocess.run(["gcc", "-std=c11", "-fsyntax-only", "-x", "c", "-",
+                        "-I" + os.path.join(ROOT, "include"), "-I/usr/local/cuda/include"],
+                       input=src, text=True, capture_output=True)
+    assert r.returncode == 0, r.stderr
+
+
+def _prefill(**kw):
+    a = dict(q=16, k=16, v=16, o=16, lse=None, B=1, H=1, S_q=8, S_kv=8, D=64, layout=0, dtype=0,
+             causal=0, scale=0.125, stream=None)
+    a.update(kw)
+    return attn.attn_prefill_fwd(**a)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(D=96), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(D=256), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(B=-1), attn.ATTN_ERR_INVALID_ARG),
+    (dict(S_kv=-3), attn.ATTN_ERR_INVALID_ARG),
+    (dict(layout=2), attn.ATTN_ERR_INVALID_ARG),
+    (dict(dtype=7), attn.ATTN_ERR_INVALID_ARG),
+    (dict(causal=2), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=0.0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=-1.0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), attn.ATTN_ERR_INVALID_ARG),
+    (dict(q=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(o=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(k=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(q=8), attn.ATTN_ERR_INVALID_ARG),  # not 16-byte aligned
+])
+def test_prefill_rejects_bad_arguments(kw, code):
+    assert _prefill(**kw) == code
+    assert attn.attn_last_error()
+
+
+def test_prefill_empty_problem_is_a_no_op():
+    assert _prefill(B=0, q=None, k=None, v=None, o=None) == attn.ATTN_OK
+    assert _prefill(S_q=0) == attn.ATTN_OK
+    assert _prefill(H=0) == attn.ATTN_OK
+
+
+def _decode(**kw):
+    a = dict(q=16, k_pool=16, v_pool=16, page_table=None, kv_lens=16, o=16, B=2, H_q=8, H_kv=2,
+             D=128, page_size=64, max_pages_per_seq=1, num_pages=2, num_splits=0, scale=0.1,
+             dtype=1, stream=None)
+    a.update(kw)
+    return attn.attn_decode_fwd(**a)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(H_kv=3), attn.ATTN_ERR_INVALID_ARG),
+    (dict(H_q=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(H_q=64, H_kv=2), attn.ATTN_ERR_UNSUPPORTED),  # group of 32 > 16
+    (dict(D=80), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(dtype=3), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=0.0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(num_splits=-1), attn.ATTN_ERR_INVALID_ARG),
+    (dict(page_size=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(num_pages=3), attn.ATTN_ERR_INVALID_ARG),  # contiguous: num_pages must be B
+    (dict(page_table=16, page_size=24, max_pages_per_seq=4, num_pages=9),
+     attn.ATTN_ERR_UNSUPPORTED),
+    (dict(page_table=16, page_size=16, max_pages_per_seq=0, num_pages=9),
+     attn.ATTN_ERR_INVALID_ARG),
+    (dict(kv_lens=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(o=4), attn.ATTN_ERR_INVALID_ARG),  # misaligned
+])
+def test_decode_rejects_bad_arguments(kw, code):
+    assert _decode(**kw) == code
+    assert attn.attn_last_error()
+
+
+def test_decode_empty_batch_is_a_no_op():
+    assert _decode(B=0, num_pages=0) == attn.ATTN_OK
+
+
+def test_product_never_imports_the_oracle():
+    pkg = os.path.join(ROOT, "attention_flash_attn_fwd_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h")):
+                with open(os.path.join(dirpath, fn)) as f:
+                    text = f.read()
+                for bad in ("import oracle", "from oracle", "liboracle", "attn_oracle"):
+                    assert bad not in text, (fn, bad)

@@ -1,0 +1,169 @@
+"""Decode (split-KV, paged/contiguous, GQA) parity against the float64 oracle."""
+import pytest
+import torch
+
+import attention_flash_attn_fwd_gb300 as attn
+import oracle
+import workloads
+from parity import assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu(inp: workloads.DecodeInputs, num_splits=0, scale=None):
+    pt = inp.page_table.cuda() if inp.page_table is not None else None
+    o = attn.decode(inp.q.cuda(), inp.k.cuda(), inp.v.cuda(), inp.kv_lens.cuda(), page_table=pt,
+                    num_splits=num_splits, scale=scale)
+    torch.cuda.synchronize()
+    assert attn.attn_device_error() == 0
+    return o.cpu()
+
+
+def _ref(inp, scale):
+    o, _ = oracle.decode(inp.q, inp.k, inp.v, inp.kv_lens, scale=scale, page_table=inp.page_table)
+    return o
+
+
+@pytest.mark.parametrize("paged", [False, True])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("H_q,H_kv", [(8, 2), (32, 8), (4, 4), (16, 1)])
+@pytest.mark.parametrize("num_splits", [0, 1, 3])
+def test_decode_matches_oracle(num_splits, H_q, H_kv, D, dtype, paged):
+    case = workloads.DecodeCase("t", 4, H_q, H_kv, D, 1, 700, 704, paged=paged, page_size=16,
+                                dtype=dtype, seed=2)
+    inp = workloads.make_decode(case, kv_lens=[1, 17, 700, 64])
+    out = _gpu(inp, num_splits=num_splits, scale=case.scale)
+    assert_close(out, _ref(inp, case.scale), "decode %s" % case)
+
+
+@pytest.mark.parametrize("page_size", [8, 16, 32, 64, 128])
+def test_decode_page_sizes(page_size):
+    case = workloads.DecodeCase("t", 3, 8, 2, 128, 1, 1000, 1024, paged=True, page_size=page_size,
+                                seed=4)
+    inp = workloads.make_decode(case, kv_lens=[1000, 129, 63])
+    out = _gpu(inp, scale=case.scale)
+    assert_close(out, _ref(inp, case.scale), "page_size %d" % page_size)
+
+
+@pytest.mark.parametrize("kv", [1, 15, 16, 17, 63, 64, 65, 127, 128, 1000])
+def test_decode_length_edges(kv):
+    case = workloads.DecodeCase("t", 2, 8, 2, 128, 1, 1024, 1024, paged=True, seed=5)
+    inp = workloads.make_decode(case, kv_lens=[kv, 1024 - kv + 1])
+    for ns in (0, 2):
+        out = _gpu(inp, num_splits=ns, scale=case.scale)
+        assert_close(out, _ref(inp, case.scale), "kv=%d splits=%d" % (kv, ns))
+
+
+def test_decode_zero_length_sequence_gives_zero():
+    case = workloads.DecodeCase("t", 3, 8, 2, 128, 0, 0, 256, paged=True, seed=6)
+    inp = workloads.make_decode(case, kv_lens=[0, 100, 0])
+    out = _gpu(inp, scale=case.scale)
+    assert torch.all(out[0] == 0) and torch.all(out[2] == 0)
+    assert_close(out, _ref(inp, case.scale), "zero-length")
+
+
+def test_decode_ignores_non_finite_page_tails():
+    """Tail slots and unused pages hold NaN/inf: only keys < kv_len may matter."""
+    case = workloads.DecodeCase("t", 3, 8, 2, 128, 1, 500, 512, paged=True, seed=7)
+    inp = workloads.make_decode(case, kv_lens=[3, 250, 499])
+    ref = _ref(inp, case.scale)
+    k, v = inp.k.clone(), inp.v.clone()
+    poison = torch.tensor(workloads.POISON).to(k.dtype)
+    k[k == poison] = float("nan")
+    v[v == poison] = float("inf")
+    bad = workloads.DecodeInputs(inp.q, k, v, inp.kv_lens, inp.page_table, inp.page_size,
+                                 inp.max_pages)
+    out = _gpu(bad, scale=case.scale)
+    assert torch.isfinite(out.float()).all()
+    assert_close(out, ref, "poisoned tails")
+    cont = workloads.contiguous_view_of(inp)
+    kc, vc = cont.k.clone(), cont.v.clone()
+    kc[kc == poison] = float("nan")
+    vc[vc == poison] = float("nan")
+    out_c = _gpu(workloads.DecodeInputs(cont.q, kc, vc, cont.kv_lens, None, cont.page_size, 1),
+                 scale=case.scale)
+    assert_close(out_c, ref, "poisoned contiguous rows")
+
+
+def test_paged_equals_contiguous_bitwise():
+    case = workloads.DecodeCase("t", 5, 32, 8, 128, 1, 3000, 3072, paged=True, seed=8)
+    inp = workloads.make_decode(case)
+    cont = workloads.contiguous_view_of(inp)
+    for ns in (0, 1, 4):
+        assert torch.equal(_gpu(inp, num_splits=ns, scale=case.scale),
+                           _gpu(cont, num_splits=ns, scale=case.scale))
+
+
+def test_split_count_does_not_change_result():
+    case = workloads.DecodeCase("t", 3, 16, 4, 128, 2000, 6000, 6144, paged=False, seed=9)
+    inp = workloads.make_decode(case)
+    ref = _ref(inp, case.scale)
+    outs = [_gpu(inp, num_splits=ns, scale=case.scale) for ns in (1, 2, 7, 0)]
+    for o in outs:
+        assert_close(o, ref, "splits")
+    for o in outs[1:]:
+        assert (o.float() - outs[0].float()).abs().max().item() <= 1e-2
+
+
+def test_decode_equals_prefill_row():
+    """Decode of one query == a one-row (S_q = 1) prefill over the same keys."""
+    case = workloads.DecodeCase("t", 1, 8, 8, 128, 777, 777, 777, paged=False, seed=10)
+    inp = workloads.make_decode(case)
+    out = _gpu(inp, scale=case.scale)
+    q = inp.q.view(1, 1, 8, 128).cuda()  # BSHD with S_q = 1
+    pre = attn.prefill(q, inp.k.cuda(), inp.v.cuda(), layout="bshd", scale=case.scale)
+    torch.cuda.synchronize()
+    assert (pre.view(1, 8, 128).cpu().float() - out.float()).abs().max().item() <= 1e-2
+
+
+def test_decode_is_deterministic():
+    case = workloads.DecodeCase("t", 4, 32, 8, 128, 100, 4000, 4096, paged=True, seed=11)
+    inp = workloads.make_decode(case)
+    assert torch.equal(_gpu(inp, scale=case.scale), _gpu(inp, scale=case.scale))
+
+
+# ------------------------------------------------------------ full size
+
+
+@pytest.fixture(scope="module")
+def contiguous_full():
+    return workloads.make_decode(workloads.C4)
+
+
+@pytest.fixture(scope="module")
+def paged_full():
+    return workloads.make_decode(workloads.C5)
+
+
+def _check_sampled(inp, out, bs, scale):
+    for b in bs:
+        n = int(inp.kv_lens[b])
+        if inp.page_table is None:
+            sub = workloads.DecodeInputs(inp.q[b:b + 1], inp.k[b:b + 1, :n], inp.v[b:b + 1, :n],
+                                         inp.kv_lens[b:b + 1], None, n, 1)
+        else:  # the sequence's own pages, in table order (data movement only)
+            pages = inp.page_table[b, : -(-n // inp.page_size)].long()
+            sub = workloads.DecodeInputs(inp.q[b:b + 1], inp.k[pages], inp.v[pages],
+                                         inp.kv_lens[b:b + 1],
+                                         torch.arange(len(pages), dtype=torch.int32).view(1, -1),
+                                         inp.page_size, len(pages))
+        assert_close(out[b:b + 1], _ref(sub, scale), "b=%d kv=%d" % (b, n))
+
+
+def test_full_size_contiguous_sampled(contiguous_full):
+    inp = contiguous_full
+    out = _gpu(inp, scale=workloads.C4.scale)
+    assert torch.isfinite(out.float()).all()
+    lens = inp.kv_lens.tolist()
+    bs = sorted({0, lens.index(max(lens)), lens.index(min(lens)), 31})
+    _check_sampled(inp, out, bs, workloads.C4.scale)
+
+
+def test_full_size_paged_sampled(paged_full):
+    inp = paged_full
+    out = _gpu(inp, scale=workloads.C5.scale)
+    assert torch.isfinite(out.float()).all()
+    lens = inp.kv_lens.tolist()
+    bs = sorted({1, lens.index(max(lens)), lens.index(min(lens)), 30})
+    _check_sampled(inp, out, bs, workloads.C5.scale)

@@ -1,0 +1,148 @@
+"""Prefill kernel parity against the float64 oracle, through the C ABI."""
+import math
+
+import pytest
+import torch
+
+import attention_flash_attn_fwd_gb300 as attn
+import oracle
+import workloads
+from parity import assert_close, assert_lse_close
+
+pytestmark = pytest.mark.gpu
+
+LAYOUT = {"bhsd": oracle.BHSD, "bshd": oracle.BSHD}
+
+
+def _run(case: workloads.PrefillCase):
+    q, k, v = workloads.make_prefill(case)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o, lse = attn.prefill(qd, kd, vd, causal=case.causal, scale=case.scale, layout=case.layout,
+                          return_lse=True)
+    torch.cuda.synchronize()
+    assert attn.attn_device_error() == 0
+    return (q, k, v), o, lse
+
+
+def _check_full(case):
+    (q, k, v), o, lse = _run(case)
+    ref_o, ref_lse = oracle.prefill(q, k, v, causal=case.causal, scale=case.scale,
+                                    layout=LAYOUT[case.layout])
+    assert_close(o, ref_o, case.name)
+    assert_lse_close(lse, ref_lse, case.name)
+    return o, lse
+
+
+def test_tiny_config_matches_oracle():
+    """B=1, H=2, S=128, D=64, BHSD fp16, non-causal, scale 1/8, seed 0."""
+    _check_full(workloads.C1)
+
+
+_SHAPES = [  # (B, H, S_q, S_kv): ragged tails, several CTAs, S_q != S_kv
+    (1, 2, 300, 300),
+    (2, 3, 513, 513),
+    (1, 2, 100, 700),
+    (1, 1, 700, 260),
+    (1, 1, 1, 1),
+    (1, 2, 129, 1000),
+]
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("layout", ["bhsd", "bshd"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", _SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_prefill_sweep_matches_oracle(shape, causal, layout, dtype, D):
+    B, H, S_q, S_kv = shape
+    case = workloads.PrefillCase("sweep", B, H, S_q, S_kv, D, layout, dtype, causal, seed=11)
+    _check_full(case)
+
+
+def test_empty_kv_gives_zero_and_neg_inf_lse():
+    q = torch.randn(1, 2, 40, 64, dtype=torch.float16, device="cuda")
+    k = torch.empty(1, 2, 0, 64, dtype=torch.float16, device="cuda")
+    o, lse = attn.prefill(q, k, k, return_lse=True)
+    torch.cuda.synchronize()
+    assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
+
+
+def test_constant_v_and_causal_row_zero():
+    g = torch.Generator().manual_seed(5)
+    q = torch.randn(2, 4, 384, 128, generator=g).to(torch.bfloat16).cuda()
+    k = torch.randn(2, 4, 384, 128, generator=g).to(torch.bfloat16).cuda()
+    v = torch.full((2, 4, 384, 128), 0.75, dtype=torch.bfloat16, device="cuda")
+    o = attn.prefill(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    assert (o.float() - 0.75).abs().max().item() <= 4e-3
+    v2 = torch.randn(2, 4, 384, 128, generator=g).to(torch.bfloat16).cuda()
+    o2 = attn.prefill(q, k, v2, causal=True)
+    torch.cuda.synchronize()
+    # Row 0 sees only key 0: its weight is exactly 1, so O[0] == V[0] bit for bit.
+    assert torch.equal(o2[:, :, 0], v2[:, :, 0])
+
+
+def test_zero_q_gives_mean_of_visible_v():
+    g = torch.Generator().manual_seed(6)
+    S = 260
+    k = torch.randn(1, 2, S, 64, generator=g).to(torch.float16)
+    v = torch.randn(1, 2, S, 64, generator=g).to(torch.float16)
+    q = torch.zeros(1, 2, S, 64, dtype=torch.float16)
+    o, lse = attn.prefill(q.cuda(), k.cuda(), v.cuda(), causal=True, return_lse=True)
+    torch.cuda.synchronize()
+    counts = torch.arange(1, S + 1, dtype=torch.float64)
+    mean = v.double().cumsum(dim=2) / counts.view(1, 1, S, 1)
+    assert_close(o, mean, "zero-q causal mean")
+    assert_lse_close(lse, torch.log(counts).view(1, 1, S).expand(1, 2, S), "zero-q lse")
+
+
+def test_prefill_is_deterministic():
+    case = workloads.PrefillCase("det", 2, 4, 640, 640, 128, "bhsd", "bf16", True, seed=3)
+    q, k, v = (t.cuda() for t in workloads.make_prefill(case))
+    o1 = attn.prefill(q, k, v, causal=True)
+    o2 = attn.prefill(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2)
+
+
+def test_layouts_agree_bitwise():
+    case = workloads.PrefillCase("lay", 2, 3, 333, 333, 128, "bhsd", "fp16", True, seed=4)
+    q, k, v = (t.cuda() for t in workloads.make_prefill(case))
+    o1 = attn.prefill(q, k, v, causal=True, layout="bhsd")
+    t = lambda x: x.transpose(1, 2).contiguous()  # noqa: E731
+    o2 = attn.prefill(t(q), t(k), t(v), causal=True, layout="bshd")
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2.transpose(1, 2))
+
+
+def _sampled_heads(case, heads):
+    """Run a full-size case on the GPU; check chosen (b, h) heads in full against the oracle."""
+    q, k, v = workloads.make_prefill(case)
+    o, lse = attn.prefill(q.cuda(), k.cuda(), v.cuda(), causal=case.causal, scale=case.scale,
+                          layout=case.layout, return_lse=True)
+    torch.cuda.synchronize()
+    assert attn.attn_device_error() == 0
+    o = o.cpu()
+    lse = lse.cpu()
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+    for b, h in heads:
+        if case.layout == "bhsd":
+            sl = lambda x: x[b:b + 1, h:h + 1]  # noqa: E731
+        else:
+            sl = lambda x: x[b:b + 1, :, h:h + 1]  # noqa: E731
+        ref_o, ref_lse = oracle.prefill(sl(q), sl(k), sl(v), causal=case.causal, scale=case.scale,
+                                        layout=LAYOUT[case.layout])
+        assert_close(sl(o), ref_o, "%s b=%d h=%d" % (case.name, b, h))
+        assert_lse_close(lse[b:b + 1, h:h + 1], ref_lse, "%s lse" % case.name)
+
+
+def test_full_size_bhsd_fp16_noncausal_sampled():
+    _sampled_heads(workloads.C2, [(0, 0), (3, 31)])
+
+
+def test_full_size_bhsd_fp16_causal_sampled():
+    _sampled_heads(workloads.C2_CAUSAL, [(1, 7), (3, 30)])
+
+
+def test_full_size_bshd_bf16_causal_sampled():
+    _sampled_heads(workloads.C3, [(0, 0), (7, 39), (4, 21)])
