@@ -22,7 +22,17 @@ constexpr uint64_t kDefaultWaitLimitNs = 4000000000ull;  // 4 s
 constexpr int kMaxDevices = 64;
 
 thread_local std::string t_last_error;
-std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitLimitNs};
+
+uint64_t initial_wait_limit() {
+  const char* v = std::getenv("ATTN_WAIT_LIMIT_NS");
+  if (v && *v) {
+    unsigned long long n = std::strtoull(v, nullptr, 10);
+    if (n > 0) return n;
+  }
+  return kDefaultWaitLimitNs;
+}
+
+std::atomic<uint64_t> g_wait_limit_ns{initial_wait_limit()};
 
 __device__ int g_device_error_word = 0;
 
@@ -122,7 +132,7 @@ const char* attn_version(void) { return "attn_gb300 0.1.0 (sm_103a)"; }
 const char* attn_last_error(void) { return t_last_error.c_str(); }
 
 void attn_set_wait_limit_ns(uint64_t ns) {
-  g_wait_limit_ns.store(ns ? ns : kDefaultWaitLimitNs);
+  g_wait_limit_ns.store(ns ? ns : initial_wait_limit());
 }
 
 attn_status attn_device_error(int* word, int clear) {

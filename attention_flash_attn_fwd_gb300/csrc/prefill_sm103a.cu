@@ -372,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     fence_proxy_async_smem();
     named_barrier_sync(1 + t, 128);
-    if (wl == 0 && lane == 0) {
+    if (wl == 0 && lane == 0 && row0 < p.S_q) {
       for (int x = 0; x < D / 64; ++x)
         if (p.bshd)
           tma_store_4d(&tm_o, s_o + x * (kBM * 128), x * 64, h, row0, b);

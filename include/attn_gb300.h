@@ -135,7 +135,8 @@ ATTN_API attn_status attn_device_error(int* word, int clear);
 
 /*
  * Set the time limit (nanoseconds) every kernel wait is bounded by; 0 restores
- * the default (4 s).  Applies to launches made after the call.
+ * the default (4 s, or the ATTN_WAIT_LIMIT_NS environment variable if set when
+ * the library was loaded).  Applies to launches made after the call.
  */
 ATTN_API void attn_set_wait_limit_ns(uint64_t ns);
 
