@@ -43,8 +43,9 @@ _STATUS_NAMES = {
 }
 
 # Names the header exports (checked against include/attn_gb300.h by the tests).
-EXPORTED = ("attn_prefill_fwd", "attn_decode_fwd", "attn_last_error", "attn_device_error",
-            "attn_set_wait_limit_ns", "attn_release_workspace", "attn_version")
+EXPORTED = ("attn_prefill_fwd", "attn_decode_fwd", "attn_decode_fwd_noalloc", "attn_last_error",
+            "attn_device_error", "attn_set_wait_limit_ns", "attn_release_workspace",
+            "attn_version")
 
 
 class AttnError(RuntimeError):
@@ -78,6 +79,8 @@ def lib() -> ctypes.CDLL:
             L.attn_decode_fwd.argtypes = [vp, vp, vp, i32p, i32p, vp, ci, ci, ci, ci, ci, ci, ci,
                                           ci, cf, ci, vp]
             L.attn_decode_fwd.restype = ci
+            L.attn_decode_fwd_noalloc.argtypes = L.attn_decode_fwd.argtypes
+            L.attn_decode_fwd_noalloc.restype = ci
             L.attn_last_error.argtypes = []
             L.attn_last_error.restype = ctypes.c_char_p
             L.attn_device_error.argtypes = [ctypes.POINTER(ctypes.c_int), ci]
@@ -118,6 +121,18 @@ def attn_decode_fwd(q, k_pool, v_pool, page_table, kv_lens, o, B, H_q, H_kv, D, 
     return lib().attn_decode_fwd(q, k_pool, v_pool, page_table, kv_lens, o, B, H_q, H_kv, D,
                                  page_size, max_pages_per_seq, num_pages, num_splits, scale,
                                  dtype, stream)
+
+
+def attn_decode_fwd_noalloc(q, k_pool, v_pool, page_table, kv_lens, o, B, H_q, H_kv, D,
+                            page_size, max_pages_per_seq, num_pages, num_splits, scale, dtype,
+                            stream) -> int:
+    """C ``attn_decode_fwd_noalloc``: decode with its split partials in the
+    library's fixed 16 MiB device array, for callers that cannot allocate
+    (graph capture, framework-owned memory pools, allocation-free serving
+    loops).  Pointers and stream as ints.  Returns the status."""
+    return lib().attn_decode_fwd_noalloc(q, k_pool, v_pool, page_table, kv_lens, o, B, H_q,
+                                         H_kv, D, page_size, max_pages_per_seq, num_pages,
+                                         num_splits, scale, dtype, stream)
 
 
 def attn_last_error() -> str:

@@ -361,3 +361,30 @@ attn_status attn_release_workspace(void) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------
+// Internal accessors for other translation units of this library (the
+// allocation-free decode entry point).  They forward to the helpers above.
+namespace attn_internal {
+
+attn_status device_info(int** err_word, int* num_sms) {
+  DeviceState* st = nullptr;
+  attn_status s = device_state(&st);
+  if (s != ATTN_OK) return s;
+  *err_word = st->err_word;
+  *num_sms = st->num_sms;
+  return ATTN_OK;
+}
+
+attn_status set_error(attn_status s, const char* msg) { return fail(s, msg); }
+
+bool encode_decode_map(CUtensorMap* m, const void* base, int num_pages, int page_size, int H_kv,
+                       int D, int box_rows, bool bf16) {
+  return decode_map(m, base, num_pages, page_size, H_kv, D, box_rows, bf16);
+}
+
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(); }
+
+int split_chunk_override() { return env_int("ATTN_DECODE_SPLIT_CHUNK", 0); }
+
+}  // namespace attn_internal

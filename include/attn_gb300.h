@@ -122,6 +122,32 @@ ATTN_API attn_status attn_decode_fwd(const void* q, const void* k_pool, const vo
                             int num_pages, int num_splits, float scale, attn_dtype dtype,
                             cudaStream_t stream);
 
+/*
+ * Decode attention that allocates no device memory (no counterpart in the
+ * paper: the pages never discuss workspace ownership).
+ *
+ * Same arguments, rules and results as attn_decode_fwd, for callers that must
+ * not let a library allocate: code being captured into a CUDA graph, engines
+ * whose framework owns all device memory through its own pool, and serving
+ * loops that must not block on the allocator at step time.  The split
+ * partials live in one fixed 16 MiB device array inside the library (held on
+ * every GPU that loads it until the process exits) instead of a cudaMalloc'd
+ * workspace; a call whose split plan needs more returns ATTN_ERR_UNSUPPORTED
+ * and launches nothing (use num_splits > 0 with fewer splits, or
+ * attn_decode_fwd).  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress); make that first call before any stream
+ * capture.  All calls share the array and it keeps the last call's contents
+ * (nothing in it needs to start at zero); calls whose kernels overlap on the
+ * GPU race on it.
+ */
+ATTN_API attn_status attn_decode_fwd_noalloc(const void* q, const void* k_pool,
+                                             const void* v_pool, const int32_t* page_table,
+                                             const int32_t* kv_lens, void* o, int B, int H_q,
+                                             int H_kv, int D, int page_size,
+                                             int max_pages_per_seq, int num_pages,
+                                             int num_splits, float scale, attn_dtype dtype,
+                                             cudaStream_t stream);
+
 /* Message describing the last error returned on the calling thread. */
 ATTN_API const char* attn_last_error(void);
 
