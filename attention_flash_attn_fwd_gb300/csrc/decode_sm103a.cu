@@ -112,50 +112,68 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------- producer
+    // The whole warp runs the loop: it keeps a window of 32 page ids in
+    // registers (lane l holds entry window_base + l, refilled with one
+    // coalesced load) and each lane issues one TMA box of the tile, so a
+    // tile costs one instruction issue instead of a dependent page-table
+    // load per page.
     if (lane == 0) {
       tma_prefetch_map(&tm_k);
       tma_prefetch_map(&tm_v);
-      const bool paged = p.page_table != nullptr;
-      const int ps = p.page_size;
-      const int box_rows = paged ? min(ps, kKeysPerTile) : kKeysPerTile;
-      const int32_t* pt = paged ? p.page_table + static_cast<size_t>(b) * p.max_pages : nullptr;
-      int issued = 0;
-      for (int it = 0; it < n_tiles; ++it) {
-        const int st = it % kStages;
-        const int round = it / kStages;
-        if (round > 0 && !mbar_wait(&empty[st], (round - 1) & 1, p.wait_limit_ns, p.err, 50))
-          break;
-        const int k0 = start + it * kKeysPerTile;
-        const int n_box = paged ? min(kKeysPerTile / box_rows, (end - k0 + box_rows - 1) / box_rows)
-                                : 1;
-        mbar_arrive_expect_tx(&full[st], 2 * C::kHalves * n_box * box_rows * 128);
-        uint8_t* kd = smem + st * C::kStageBytes;
-        uint8_t* vd = kd + C::kTileBytes;
-        for (int bx = 0; bx < n_box; ++bx) {
-          const int key = k0 + bx * box_rows;  // first logical key of this box
-          int page, slot;
-          if (paged) {
-            page = pt[key / ps];
-            slot = key % ps;
-            if (page < 0 || page >= p.num_pages) {  // TMA would zero-fill; flag it
-              record_error(p.err, kErrBadArgument, 2);
-              page = p.num_pages;
-            }
-          } else {
-            page = b;
-            slot = key;
-          }
-          for (int hf = 0; hf < C::kHalves; ++hf) {
-            const uint32_t off = hf * C::kHalfBytes + bx * box_rows * 128;
-            tma_load_4d(kd + off, &tm_k, &full[st], hf * 64, g, slot, page);
-            tma_load_4d(vd + off, &tm_v, &full[st], hf * 64, g, slot, page);
-          }
-        }
-        issued = it + 1;
+    }
+    const bool paged = p.page_table != nullptr;
+    const int ps = p.page_size;
+    const int box_rows = paged ? min(ps, kKeysPerTile) : kKeysPerTile;
+    const int boxes_per_tile = paged ? kKeysPerTile / box_rows : 1;
+    const int32_t* pt = paged ? p.page_table + static_cast<size_t>(b) * p.max_pages : nullptr;
+    const int n_pages_seq = paged ? (kv + ps - 1) / ps : 0;  // entries that may be read
+    int window_base = -(1 << 30);
+    int window_page = 0;
+    int issued = 0;
+    for (int it = 0; it < n_tiles; ++it) {
+      const int st = it % kStages;
+      const int round = it / kStages;
+      if (round > 0) {
+        const bool ok = mbar_wait(&empty[st], (round - 1) & 1, p.wait_limit_ns, p.err, 50);
+        if (!__all_sync(0xffffffffu, ok)) break;
       }
+      const int k0 = start + it * kKeysPerTile;
+      const int n_box = paged ? min(boxes_per_tile, (end - k0 + box_rows - 1) / box_rows) : 1;
+      int page = b, slot = 0;
+      const int bx = lane / (2 * C::kHalves);
+      if (paged) {
+        const int first_p = k0 / ps;
+        const int last_p = (min(k0 + kKeysPerTile, end) - 1) / ps;
+        if (last_p >= window_base + 32) {  // refill (pages only move forward)
+          window_base = first_p;
+          const int e = window_base + lane;
+          window_page = e < n_pages_seq ? pt[e] : 0;
+        }
+        const int key = k0 + min(bx, n_box - 1) * box_rows;
+        page = __shfl_sync(0xffffffffu, window_page, key / ps - window_base);
+        slot = key % ps;
+        if (page < 0 || page >= p.num_pages) {  // the TMA would zero-fill; flag it
+          if (bx < n_box) record_error(p.err, kErrBadArgument, 2);
+          page = p.num_pages;
+        }
+      } else {
+        slot = k0;
+      }
+      if (lane == 0)
+        mbar_arrive_expect_tx(&full[st], 2 * C::kHalves * n_box * box_rows * 128);
+      __syncwarp();
+      if (bx < n_box) {
+        const int hf = (lane / 2) % C::kHalves;
+        const bool is_v = lane & 1;
+        uint8_t* dst = smem + st * C::kStageBytes + (is_v ? C::kTileBytes : 0) +
+                       hf * C::kHalfBytes + bx * box_rows * 128;
+        tma_load_4d(dst, is_v ? &tm_v : &tm_k, &full[st], hf * 64, g, slot, page);
+      }
+      issued = it + 1;
+    }
+    if (lane == 0)
       for (int it = max(0, issued - kStages); it < issued; ++it)
         mbar_wait(&full[it % kStages], (it / kStages) & 1, p.wait_limit_ns, p.err, 51);
-    }
     __syncwarp();
     return;  // the producer takes no part in the final merge
   }

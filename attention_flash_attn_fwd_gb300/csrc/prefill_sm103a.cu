@@ -39,15 +39,23 @@ namespace {
 constexpr int kBM = 128;      // query rows per tile
 constexpr int kBN = 128;      // keys per KV tile
 constexpr int kTiles = 2;     // query tiles per CTA
-constexpr int kThreads = 320; // 8 softmax warps + TMA warp + MMA warp
+constexpr int kThreads = 384; // 2 softmax warpgroups + 1 warpgroup {TMA, MMA, 2 idle}
 constexpr int kWarpTma = 8;
 constexpr int kWarpMma = 9;
+// Registers are granted per warpgroup: 384 threads launch with 168 each
+// (64512 in all).  The softmax warpgroups take 224, the TMA/MMA warpgroup
+// keeps 56: 2*128*224 + 128*56 = 64512, exactly the launch total.
+constexpr int kRegsAtLaunch = 168;
+constexpr int kRegsSoftmax = 224;
+constexpr int kRegsControl = 56;
+static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsControl <= kThreads * kRegsAtLaunch,
+              "register split exceeds the block's launch allocation");
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D>
 struct Cfg {
   static constexpr int kTileBytes = kBM * D * 2;          // one Q/K/V/O tile
-  static constexpr int kStages = (D == 128) ? 4 : 8;      // KV ring depth
+  static constexpr int kStages = (D == 128) ? 5 : 10;     // KV ring depth
   static constexpr int kSmemData = kTiles * kTileBytes + kStages * kTileBytes;
   static constexpr int kSmemBytes = kSmemData + 1024 /*align*/ + 256 /*barriers*/;
   // tensor-memory columns of S_t and O_t
@@ -58,10 +66,11 @@ struct Cfg {
 struct SharedCtl {
   uint64_t q_full[kTiles];
   uint64_t s_full[kTiles];
-  uint64_t p_full[kTiles];
+  uint64_t p_half[kTiles][2];  // P_t keys [0,64) and [64,128) in tensor memory
   uint64_t o_full;
-  uint64_t kv_full[8];
-  uint64_t kv_empty[8];
+  uint64_t tmem_free;  // every softmax warp is done reading tensor memory
+  uint64_t kv_full[10];
+  uint64_t kv_empty[10];
   uint32_t tmem_base;
   int abort;
 };
@@ -75,6 +84,20 @@ __device__ __forceinline__ void load_box(void* dst, const CUtensorMap* map, uint
   else
     tma_load_4d(dst, map, bar, x, row, h, b);
 }
+
+// L2 prefetch of one 64-column box (same coordinates as load_box).
+__device__ __forceinline__ void prefetch_box(const CUtensorMap* map, int x, int row, int h, int b,
+                                             int bshd) {
+  if (bshd)
+    tma_prefetch_l2_4d(map, x, h, row, b);
+  else
+    tma_prefetch_l2_4d(map, x, row, h, b);
+}
+
+// KV tiles the producer prefetches into L2 ahead of its shared-memory loads.
+// The CTAs of one (batch, head) stream the same K/V tiles at about the same
+// time, so without it every tile load waits for a DRAM round trip.
+constexpr int kL2PrefetchTiles = 4;
 
 // Number of KV tiles a query tile [row0, row0 + kBM) must visit.
 __device__ __forceinline__ int kv_tiles_for(int row0, const PrefillParams& p) {
@@ -111,10 +134,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = bh / p.H;
   const int h = bh % p.H;
   const int row_base = qb * (kTiles * kBM);
-  int n_kv[kTiles];
-#pragma unroll
-  for (int t = 0; t < kTiles; ++t) n_kv[t] = kv_tiles_for(row_base + t * kBM, p);
-  const int n_all = max(n_kv[0], n_kv[1]);  // tile 1 never needs fewer than tile 0
+  const int n_kv0 = kv_tiles_for(row_base, p);
+  const int n_kv1 = kv_tiles_for(row_base + kBM, p);
+  auto n_kv = [&](int t) { return t == 0 ? n_kv0 : n_kv1; };  // KV tiles of query tile t
+  const int n_all = max(n_kv0, n_kv1);  // tile 1 never needs fewer than tile 0
 
   if (warp == kWarpMma) {
     tmem_alloc(&ctl->tmem_base, 512);
@@ -124,9 +147,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = 0; t < kTiles; ++t) {
       mbar_init(&ctl->q_full[t], 1);
       mbar_init(&ctl->s_full[t], 1);
-      mbar_init(&ctl->p_full[t], 4);
+      mbar_init(&ctl->p_half[t][0], 4);
+      mbar_init(&ctl->p_half[t][1], 4);
     }
     mbar_init(&ctl->o_full, 1);
+    mbar_init(&ctl->tmem_free, 8);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&ctl->kv_full[s], 1);
       mbar_init(&ctl->kv_empty[s], 1);
@@ -139,7 +164,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = ctl->tmem_base;
 
-  if (warp == kWarpTma) {
+  if (warp >= 8) {
+   // ============================================= control warpgroup
+   setmaxnreg_dec<kRegsControl>();
+   if (warp == kWarpTma) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && n_all > 0) {
       int issued = 0;  // KV loads issued so far
@@ -152,8 +180,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           load_box(s_q + t * C::kTileBytes + x * (kBM * 128), &tm_q, &ctl->q_full[t], x * 64,
                    row_base + t * kBM, h, b, p.bshd);
       }
+      for (int j = 0; j < min(n_all, kL2PrefetchTiles); ++j)
+        for (int x = 0; x < D / 64; ++x) {
+          prefetch_box(&tm_k, x * 64, j * kBN, h, b, p.bshd);
+          prefetch_box(&tm_v, x * 64, j * kBN, h, b, p.bshd);
+        }
       volatile int* abort_flag = &ctl->abort;
       for (int j = 0; j < n_all && !*abort_flag; ++j) {
+        if (j + kL2PrefetchTiles < n_all)
+          for (int x = 0; x < D / 64; ++x) {
+            prefetch_box(&tm_k, x * 64, (j + kL2PrefetchTiles) * kBN, h, b, p.bshd);
+            prefetch_box(&tm_v, x * 64, (j + kL2PrefetchTiles) * kBN, h, b, p.bshd);
+          }
 #pragma unroll
         for (int kind = 0; kind < 2; ++kind) {
           const int idx = 2 * j + kind;
@@ -181,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = 0; t < kTiles; ++t) mbar_wait(&ctl->q_full[t], 0, p.wait_limit_ns, p.err, 12);
     }
     __syncwarp();
-  } else if (warp == kWarpMma) {
+   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n_all > 0) {
       constexpr uint32_t id_s = idesc_f16(kBF16, kBM, kBN, false, false);
@@ -192,25 +230,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = 0; t < kTiles && ok; ++t)
         ok = mbar_wait(&ctl->q_full[t], 0, p.wait_limit_ns, p.err, 20);
 
+      // Descriptors are built once; inside the loops each MMA only adds a
+      // compile-time offset to a low word, so the issuing thread can feed
+      // the tensor core's short instruction queue without a dependent chain
+      // of address arithmetic.
+      const uint32_t hi_k = sdesc_hi_sw128(1024);  // K-major: 8-row groups 1024 B apart
+      const uint32_t q_lo = sdesc_lo(q_addr, 16);
+      const uint32_t k_lo = sdesc_lo(kv_addr, 16);         // K-major: leading offset unused
+      const uint32_t v_lo = sdesc_lo(kv_addr, kBN * 128);  // V: 64-column groups 16 KB apart
+      constexpr uint32_t kTileLo = C::kTileBytes >> 4;
       // S_t = Q_t K_j^T  (both operands K-major, 128-byte swizzle)
       auto issue_s = [&](int t, int st) {
-        const uint32_t qa = q_addr + t * C::kTileBytes;
-        const uint32_t ka = kv_addr + st * C::kTileBytes;
+        const uint32_t qa = q_lo + t * kTileLo;
+        const uint32_t ka = k_lo + st * kTileLo;
+        const uint32_t d = tmem + C::col_s(t);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * (kBM * 128) + (kk % 4) * 32;
-          mma_ss(tmem + C::col_s(t), sdesc_sw128(qa + off, 16, 1024),
-                 sdesc_sw128(ka + off, 16, 1024), id_s, kk > 0);
+          const uint32_t off = ((kk / 4) * (kBM * 128) + (kk % 4) * 32) >> 4;
+          mma_ss_lh(d, qa + off, hi_k, ka + off, hi_k, id_s, kk > 0);
         }
       };
       // O_t (+)= P_t V_j  (P from tensor memory, V MN-major, 128-byte swizzle)
-      auto issue_pv = [&](int t, int st, bool acc) {
-        const uint32_t va = kv_addr + st * C::kTileBytes;
+      // Half `hf` covers keys [64*hf, 64*hf + 64): P columns [32*hf, 32*hf + 32).
+      auto issue_pv_half = [&](int t, int st, bool acc, int hf) {
+        const uint32_t va = v_lo + st * kTileLo;
+        const uint32_t d = tmem + C::col_o(t);
+        const uint32_t a = tmem + C::col_s(t);
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8,
-                 sdesc_sw128(va + kk * 16 * 128, kBN * 128, 1024), id_o,
-                 (acc || kk > 0) ? 1u : 0u);
+        for (int k4 = 0; k4 < kBN / 32; ++k4) {
+          const int kk = hf * (kBN / 32) + k4;
+          mma_ts_lh(d, a + kk * 8, va + ((kk * 16 * 128) >> 4), hi_k, id_o,
+                    (acc || kk > 0) ? 1u : 0u);
+        }
       };
       auto wait_full = [&](int idx, int site) {
         return mbar_wait(&ctl->kv_full[idx % C::kStages], (idx / C::kStages) & 1,
@@ -220,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok && (ok = wait_full(0, 21))) {
         tc_fence_after_sync();
         for (int t = 0; t < kTiles; ++t)
-          if (n_kv[t] > 0) {
+          if (n_kv(t) > 0) {
             issue_s(t, 0);
             mma_commit(&ctl->s_full[t]);
           }
@@ -233,10 +284,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool kn_ready = false;
         if (!(ok = wait_full(2 * j + 1, 22))) break;
         for (int t = 0; t < kTiles && ok; ++t) {
-          if (j < n_kv[t]) {
-            if (!(ok = mbar_wait(&ctl->p_full[t], j & 1, p.wait_limit_ns, p.err, 23 + t))) break;
-            tc_fence_after_sync();
-            issue_pv(t, st_v, j > 0);
+          if (j < n_kv(t)) {
+            for (int hf = 0; hf < 2 && ok; ++hf) {
+              ok = mbar_wait(&ctl->p_half[t][hf], j & 1, p.wait_limit_ns, p.err, 23 + 2 * t + hf);
+              if (!ok) break;
+              tc_fence_after_sync();
+              issue_pv_half(t, st_v, j > 0, hf);
+            }
+            if (!ok) break;
           }
           if (t == kTiles - 1) mma_commit(&ctl->kv_empty[st_v]);
           if (next) {
@@ -245,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               kn_ready = true;
               tc_fence_after_sync();
             }
-            if (j + 1 < n_kv[t]) {
+            if (j + 1 < n_kv(t)) {
               issue_s(t, st_kn);
               mma_commit(&ctl->s_full[t]);
             }
@@ -259,8 +314,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(&ctl->o_full, 0, p.wait_limit_ns, p.err, 26);
     }
     __syncwarp();
+    // Release tensor memory once every softmax warp has read its last O.
+    mbar_wait(&ctl->tmem_free, 0, p.wait_limit_ns, p.err, 27);
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 512);
+   }
   } else {
-    // ------------------------------------------------------------ softmax
+    // ============================================= softmax warpgroups
+    setmaxnreg_inc<kRegsSoftmax>();
     const int t = warp / 4;             // query tile of this warpgroup
     const int wl = warp % 4;            // warp's TMEM lane quarter
     const int r = wl * 32 + lane;       // row within the tile
@@ -275,14 +336,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m2 = -INFINITY;  // running reference max, scaled log2 units
     float l = 0.f;         // running sum of exponentials relative to m2
     bool ok = true;
-    for (int j = 0; j < n_kv[t]; ++j) {
+    for (int j = 0; j < n_kv(t); ++j) {
       ok = __all_sync(0xffffffffu,
                       mbar_wait(&ctl->s_full[t], j & 1, p.wait_limit_ns, p.err, 30 + t));
       if (!ok) break;
       tc_fence_after_sync();
       float s[kBN];
-      tmem_ld64_wait(lane_addr + col_s, *reinterpret_cast<float(*)[64]>(&s[0]));
-      tmem_ld64_wait(lane_addr + col_s + 64, *reinterpret_cast<float(*)[64]>(&s[64]));
+      tmem_ld128_wait(lane_addr + col_s, s);
       const int key0 = j * kBN;
       const bool full = (key0 + kBN <= p.S_kv) && (!p.causal || key0 + kBN - 1 <= row0 + diag);
       if (!full) {
@@ -291,16 +351,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int cc = 0; cc < kBN; ++cc)
           if (key0 + cc > lim) s[cc] = -INFINITY;
       }
-      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+      // Row max: eight independent chains of 3-input max, then a short tree.
+      float mx[8];
 #pragma unroll
-      for (int cc = 4; cc < kBN; cc += 4) {
-        mx0 = fmaxf(mx0, s[cc]);
-        mx1 = fmaxf(mx1, s[cc + 1]);
-        mx2 = fmaxf(mx2, s[cc + 2]);
-        mx3 = fmaxf(mx3, s[cc + 3]);
-      }
-      const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
-      const float m_new = fmaxf(m2, m_tile);
+      for (int q = 0; q < 8; ++q) mx[q] = fmax3(s[3 * q], s[3 * q + 1], s[3 * q + 2]);  // 0..23
+#pragma unroll
+      for (int cc = 24; cc < kBN - 8; cc += 16)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) mx[q] = fmax3(mx[q], s[cc + 2 * q], s[cc + 2 * q + 1]);
+      // columns 24 .. 119 consumed; 120 .. 127 remain
+#pragma unroll
+      for (int q = 0; q < 8; ++q) mx[q] = fmaxf(mx[q], s[kBN - 8 + q]);
+      const float m_raw = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                                fmaxf(mx[6], mx[7]));
+      const float m_new = fmaxf(m2, m_raw * c);
       float alpha = 1.f;
       bool need = false;
       if (m_new > m2 + kRescaleThreshold) {  // false while m_new == -inf
@@ -308,24 +372,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         need = (j > 0);
         m2 = m_new;
       }
-      const float mref = (m2 == -INFINITY) ? 0.f : m2;
-      float sum0 = 0.f, sum1 = 0.f;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int q = 0; q < 32; ++q) {
-          const float e0 = ex2_approx(fmaf(s[half * 64 + 2 * q], c, -mref));
-          const float e1 = ex2_approx(fmaf(s[half * 64 + 2 * q + 1], c, -mref));
-          sum0 += e0;
-          sum1 += e1;
-          pk[q] = pack2<kBF16>(e0, e1);
-        }
-        tmem_st32(lane_addr + col_s + half * 32, pk);
-      }
-      l = l * alpha + (sum0 + sum1);
       if (__any_sync(0xffffffffu, need)) {
-        // O_t row *= alpha.  PV_t,j-1 completed before S_t,j was signalled.
+        // O_t row *= alpha before any of P_t,j is published.  PV_t,j-1
+        // completed before S_t,j was signalled.
 #pragma unroll 1
         for (int cc = 0; cc < D; cc += 32) {
           uint32_t o[32];
@@ -335,23 +384,49 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32(lane_addr + col_o + cc, o);
         }
       }
-      tmem_st_wait();
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->p_full[t]);
+      const float mref = (m2 == -INFINITY) ? 0.f : m2;
+      const uint64_t c2 = f2_pack(c, c);
+      const uint64_t nm2 = f2_pack(-mref, -mref);
+      uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(s[half * 64 + 2 * q], s[half * 64 + 2 * q + 1]), c2, nm2), x0,
+                    x1);
+          const float e0 = ex2_approx(x0);
+          const float e1 = ex2_approx(x1);
+          if (q & 1)
+            acc1 = f2_add(acc1, f2_pack(e0, e1));
+          else
+            acc0 = f2_add(acc0, f2_pack(e0, e1));
+          pk[q] = pack2<kBF16>(e0, e1);
+        }
+        tmem_st32(lane_addr + col_s + half * 32, pk);
+        tmem_st_wait();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->p_half[t][half]);
+      }
+      float a0, a1, b0, b1;
+      f2_unpack(acc0, a0, a1);
+      f2_unpack(acc1, b0, b1);
+      l = l * alpha + ((a0 + a1) + (b0 + b1));
     }
 
     // ------------------------------------------------------------ epilogue
     if (ok && n_all > 0)
       ok = __all_sync(0xffffffffu, mbar_wait(&ctl->o_full, 0, p.wait_limit_ns, p.err, 40 + t));
     tc_fence_after_sync();
-    const bool have_o = ok && n_kv[t] > 0 && l > 0.f;
+    const bool have_o = ok && n_kv(t) > 0 && l > 0.f;
     const float inv_l = have_o ? 1.f / l : 0.f;
     uint8_t* s_o = s_q + t * C::kTileBytes;  // Q_t is dead once o_full fired
 #pragma unroll 1
     for (int cc = 0; cc < D; cc += 64) {
       uint32_t o[64] = {};
-      if (n_kv[t] > 0 && ok) tmem_ld64_wait(lane_addr + col_o + cc, o);
+      if (n_kv(t) > 0 && ok) tmem_ld64_wait(lane_addr + col_o + cc, o);
       uint8_t* sub = s_o + (cc / 64) * (kBM * 128) + r * 128;
 #pragma unroll
       for (int q = 0; q < 8; ++q) {  // 8 chunks of 8 columns = 16 bytes each
@@ -366,6 +441,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<uint4*>(sub + ((q ^ (r & 7)) * 16)) = w;
       }
     }
+    tc_fence_before_sync();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl->tmem_free);
     if (p.lse != nullptr && i < p.S_q) {
       const float lse = have_o ? (m2 + __log2f(l)) * 0.69314718055994531f : -INFINITY;
       p.lse[(static_cast<size_t>(b) * p.H + h) * p.S_q + i] = lse;
@@ -384,12 +462,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   }
 
-  tc_fence_before_sync();
-  __syncthreads();
-  if (warp == kWarpMma) {
-    tc_fence_after_sync();
-    tmem_dealloc(tmem, 512);
-  }
 }
 
 }  // namespace
@@ -401,8 +473,14 @@ static cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const 
   auto kern = prefill_fwd_kernel<D, kBF16>;
   static bool configured = false;  // per template instance
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg<D>::kSmemBytes);
+    // The in-kernel register split assumes exactly kRegsAtLaunch registers
+    // per thread at launch; with fewer, setmaxnreg.inc would never complete.
+    cudaFuncAttributes fa{};
+    cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != kRegsAtLaunch) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg<D>::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured = true;
   }
