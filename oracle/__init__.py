@@ -17,7 +17,10 @@ are stated at the top of ``attn_oracle.c``:
 * decode: one query per head against a sequence's first ``kv_len`` keys read
   through a page table, grouped-query heads ``g = h // (H_q // H_kv)``
   (Wave February 2025 Release, FlashDecoding list: paged flash decoding and
-  the fake-page-table test fixture).
+  the fake-page-table test fixture);
+* extend: S_q new queries per sequence against its ``kv_len`` keys in the
+  paged pool, bottom-right causal per sequence (Wave February 2025 Release,
+  "Extend Attention"; WAVE MLSys 2026 summary, Integration: SGLang extend).
 
 Every function here is pinned by ``tests/test_oracle.py`` against library
 routines, closed forms and analytic fixtures; no part is left unpinned.
@@ -76,6 +79,9 @@ def _load():
             lib.oracle_decode_f64.argtypes = [dp, dp, dp, ip, ip, dp, dp, L, L, L,
                                               L, L, L, ctypes.c_double, ctypes.c_int]
             lib.oracle_decode_f64.restype = ctypes.c_int
+            lib.oracle_extend_f64.argtypes = [dp, dp, dp, ip, ip, dp, dp, L, L, L, L, L, L,
+                                              L, ctypes.c_int, ctypes.c_double, ctypes.c_int]
+            lib.oracle_extend_f64.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -177,4 +183,29 @@ def decode(q, k_pool, v_pool, kv_lens, *, scale: float, page_table=None,
                                    float(scale), int(n_threads or default_threads()))
     if rc != 0:
         raise RuntimeError("oracle_decode_f64 failed (rc=%d)" % rc)
+    return o, lse
+
+
+def extend(q, k_pool, v_pool, page_table, kv_lens, *, causal: bool, scale: float,
+           n_threads: int | None = None):
+    """Prefill of S_q new queries per sequence against a paged KV cache, float64.
+
+    ``q``: [B,S_q,H_q,D]; ``k_pool``/``v_pool``: [num_pages, page_size, H_kv, D];
+    ``page_table``: [B, max_pages] int32; ``kv_lens``: [B] int32 (cached keys
+    including the new tokens).  Returns ``(o [B,S_q,H_q,D], lse [B,H_q,S_q])``.
+    """
+    q64, k64, v64 = _f64(q), _f64(k_pool), _f64(v_pool)
+    pt, lens = _i32(page_table), _i32(kv_lens)
+    B, S_q, H_q, D = q64.shape
+    _, page_size, H_kv, D2 = k64.shape
+    if D2 != D or v64.shape != k64.shape or pt.ndim != 2 or pt.shape[0] != B:
+        raise ValueError("shape mismatch")
+    o = np.zeros(q64.shape, dtype=np.float64)
+    lse = np.zeros((B, H_q, S_q), dtype=np.float64)
+    rc = _load().oracle_extend_f64(_dptr(q64), _dptr(k64), _dptr(v64), _iptr(pt), _iptr(lens),
+                                   _dptr(o), _dptr(lse), B, S_q, H_q, H_kv, D, page_size,
+                                   pt.shape[1], int(bool(causal)), float(scale),
+                                   int(n_threads or default_threads()))
+    if rc != 0:
+        raise RuntimeError("oracle_extend_f64 failed (rc=%d)" % rc)
     return o, lse

@@ -39,6 +39,13 @@
  *     pool laid out [num_pages, page_size, H_kv, D]; a NULL page table means
  *     "contiguous", i.e. page b of a pool [B, page_size, H_kv, D].
  *
+ * Extend (prefill against a paged KV cache, "Extend Attention", Wave
+ * February 2025 Release, De-Prioritized list; the SGLang "extend" mode of
+ * the WAVE MLSys 2026 summary, Integration) is the prefill definition applied
+ * to each sequence's gathered keys: S_q new queries of sequence b attend to
+ * its kv_lens[b] cached keys (which include the new tokens), causal
+ * alignment bottom-right per sequence, kv head h / (H_q / H_kv).
+ *
  * Rows are independent; they are spread over POSIX threads.
  */
 #include <math.h>
@@ -167,16 +174,18 @@ typedef struct {
 } decode_job;
 
 /* Gather sequence b's keys and values for kv head g into contiguous
- * [kv_len, D] arrays, through the page table. */
-static void gather_sequence(const decode_job *J, long b, long g, long kv_len,
-                            double *k_seq, double *v_seq) {
-    const long D = J->D;
+ * [kv_len, D] arrays, through the page table (pool [pages, page_size, H_kv,
+ * D]; a NULL page table means sequence b owns page b). */
+static void gather_sequence(const double *k_pool, const double *v_pool,
+                            const int32_t *page_table, long max_pages,
+                            long page_size, long H_kv, long D, long b, long g,
+                            long kv_len, double *k_seq, double *v_seq) {
     for (long t = 0; t < kv_len; ++t) {
-        long page = J->page_table ? (long)J->page_table[b * J->max_pages + t / J->page_size] : b;
-        long slot = t % J->page_size;
-        size_t row = (size_t)(((page * J->page_size + slot) * J->H_kv + g) * D);
-        memcpy(k_seq + t * D, J->k_pool + row, sizeof(double) * (size_t)D);
-        memcpy(v_seq + t * D, J->v_pool + row, sizeof(double) * (size_t)D);
+        long page = page_table ? (long)page_table[b * max_pages + t / page_size] : b;
+        long slot = t % page_size;
+        size_t row = (size_t)(((page * page_size + slot) * H_kv + g) * D);
+        memcpy(k_seq + t * D, k_pool + row, sizeof(double) * (size_t)D);
+        memcpy(v_seq + t * D, v_pool + row, sizeof(double) * (size_t)D);
     }
 }
 
@@ -200,7 +209,8 @@ static void *decode_worker(void *arg) {
         long b = r / J->H_q, h = r % J->H_q, g = h / group;
         long kv_len = J->kv_lens[b];
         if (b != have_b || g != have_g) {
-            gather_sequence(J, b, g, kv_len, k_seq, v_seq);
+            gather_sequence(J->k_pool, J->v_pool, J->page_table, J->max_pages,
+                            J->page_size, J->H_kv, D, b, g, kv_len, k_seq, v_seq);
             have_b = b;
             have_g = g;
         }
@@ -254,4 +264,94 @@ int oracle_decode_f64(const double *q, const double *k_pool,
     decode_job J = {q, k_pool, v_pool, page_table, kv_lens, o, lse,
                     B, H_q, H_kv, D, page_size, max_pages, scale, 0};
     return run_threads(decode_worker, &J, n_threads);
+}
+
+/* ----------------------------------------------------------------- extend */
+
+typedef struct {
+    const double *q, *k_pool, *v_pool;
+    const int32_t *page_table, *kv_lens;
+    double *o, *lse;
+    long B, S_q, H_q, H_kv, D, page_size, max_pages;
+    int causal;
+    double scale;
+    long next_row; /* shared work counter over (b, h) */
+} extend_job;
+
+static void *extend_worker(void *arg) {
+    extend_job *J = (extend_job *)arg;
+    const long D = J->D;
+    const long cap = J->max_pages * J->page_size;
+    double *k_seq = (double *)malloc(sizeof(double) * (size_t)(cap * D + 1));
+    double *v_seq = (double *)malloc(sizeof(double) * (size_t)(cap * D + 1));
+    double *s_buf = (double *)malloc(sizeof(double) * (size_t)(cap + 1));
+    if (!k_seq || !v_seq || !s_buf) {
+        free(k_seq); free(v_seq); free(s_buf);
+        return (void *)1;
+    }
+    const long group = J->H_q / J->H_kv;
+    const long total = J->B * J->H_q;
+    for (;;) {
+        long r = __atomic_fetch_add(&J->next_row, 1, __ATOMIC_RELAXED);
+        if (r >= total) break;
+        const long b = r / J->H_q, h = r % J->H_q, kvh = h / group;
+        const long kv_len = J->kv_lens[b];
+        gather_sequence(J->k_pool, J->v_pool, J->page_table, J->max_pages,
+                        J->page_size, J->H_kv, D, b, kvh, kv_len, k_seq, v_seq);
+        for (long i = 0; i < J->S_q; ++i) {
+            /* q and o are [B, S_q, H_q, D]; lse is [B, H_q, S_q] */
+            const double *q_row = J->q + (size_t)(((b * J->S_q + i) * J->H_q + h) * D);
+            double *o_row = J->o + (size_t)(((b * J->S_q + i) * J->H_q + h) * D);
+            double *lse_out = J->lse + (size_t)((b * J->H_q + h) * J->S_q + i);
+            long last = kv_len - 1;
+            if (J->causal) {
+                long lim = i + (kv_len - J->S_q);
+                if (lim < last) last = lim;
+            }
+            if (last < 0) {
+                for (long d = 0; d < D; ++d) o_row[d] = 0.0;
+                *lse_out = -INFINITY;
+                continue;
+            }
+            double m = -INFINITY;
+            for (long j = 0; j <= last; ++j) {
+                double dot = 0.0;
+                for (long d = 0; d < D; ++d) dot += q_row[d] * k_seq[j * D + d];
+                s_buf[j] = J->scale * dot;
+                if (s_buf[j] > m) m = s_buf[j];
+            }
+            double l = 0.0;
+            for (long d = 0; d < D; ++d) o_row[d] = 0.0;
+            for (long j = 0; j <= last; ++j) {
+                double w = exp(s_buf[j] - m);
+                l += w;
+                for (long d = 0; d < D; ++d) o_row[d] += w * v_seq[j * D + d];
+            }
+            for (long d = 0; d < D; ++d) o_row[d] /= l;
+            *lse_out = m + log(l);
+        }
+    }
+    free(k_seq);
+    free(v_seq);
+    free(s_buf);
+    return NULL;
+}
+
+/* q: [B,S_q,H_q,D]; k_pool, v_pool: [num_pages, page_size, H_kv, D];
+ * page_table: [B, max_pages] int32; kv_lens: [B] int32; o: [B,S_q,H_q,D];
+ * lse: [B,H_q,S_q].  Returns 0 on success, -1 on bad arguments. */
+int oracle_extend_f64(const double *q, const double *k_pool, const double *v_pool,
+                      const int32_t *page_table, const int32_t *kv_lens, double *o,
+                      double *lse, long B, long S_q, long H_q, long H_kv, long D,
+                      long page_size, long max_pages, int causal, double scale,
+                      int n_threads) {
+    if (B < 0 || S_q < 0 || H_q <= 0 || H_kv <= 0 || D <= 0 || page_size <= 0 || max_pages <= 0)
+        return -1;
+    if (H_q % H_kv != 0 || page_table == NULL) return -1;
+    for (long b = 0; b < B; ++b)
+        if (kv_lens[b] < 0 || kv_lens[b] > max_pages * page_size) return -1;
+    if (B == 0 || S_q == 0) return 0;
+    extend_job J = {q, k_pool, v_pool, page_table, kv_lens, o, lse, B, S_q, H_q, H_kv, D,
+                    page_size, max_pages, causal, scale, 0};
+    return run_threads(extend_worker, &J, n_threads);
 }

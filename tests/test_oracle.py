@@ -5,7 +5,8 @@ itself: analytic fixtures (tests/golden), PyTorch's own float64
 scaled_dot_product_attention and logsumexp, closed forms (Q=0, constant V,
 causal row 0, a single key, rows summing to 1) and structural invariants
 (layout swap, key permutation, GQA == repeated heads, paged == contiguous,
-decode == a one-row prefill).  ``test_mutants_are_caught`` plants plausible
+decode == a one-row prefill, extend == per-sequence prefill against the
+gathered pages, and a pure-Python brute force of extend).  ``test_mutants_are_caught`` plants plausible
 mistakes in a copy of the oracle's C source and checks the pins fail.
 """
 import glob
@@ -280,18 +281,129 @@ def test_oracle_rejects_bad_arguments():
         oracle.decode(np.zeros((1, 2, 4)), k, k, np.array([5]), scale=1.0)
 
 
+# ------------------------------------------------------------------ extend
+
+
+def _extend_torch_ref(inp, causal, scale):
+    """Per sequence: gather its kv_len keys through the page table with torch
+    indexing, repeat kv heads for GQA and call PyTorch float64 SDPA with an
+    explicit bottom-right mask."""
+    B, S_q, H_q, D = inp.q.shape
+    H_kv = inp.k.shape[2]
+    ps = inp.page_size
+    outs, lses = [], []
+    for b in range(B):
+        n = int(inp.kv_lens[b])
+        t = torch.arange(n)
+        phys = inp.page_table[b].long()[t // ps]
+        kb = inp.k[phys, t % ps].double().permute(1, 0, 2).repeat_interleave(H_q // H_kv, 0)[None]
+        vb = inp.v[phys, t % ps].double().permute(1, 0, 2).repeat_interleave(H_q // H_kv, 0)[None]
+        qb = inp.q[b].double().permute(1, 0, 2)[None]  # [1, H_q, S_q, D]
+        mask = _bottom_right(S_q, n) if causal else torch.ones(S_q, n, dtype=torch.bool)
+        o = F.scaled_dot_product_attention(qb, kb, vb, attn_mask=mask, scale=scale)
+        lse = _lse_ref(qb, kb, scale, mask)
+        empty = ~mask.any(dim=1)  # rows with no visible key: o = 0 by definition
+        o[:, :, empty] = 0.0
+        outs.append(o[0].permute(1, 0, 2))
+        lses.append(lse[0])
+    return torch.stack(outs), torch.stack(lses)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("H_q,H_kv,page_size", [(4, 4, 16), (8, 2, 8), (6, 1, 64)])
+def test_extend_matches_torch_sdpa(causal, H_q, H_kv, page_size):
+    case = workloads.ExtendCase("t", 3, 21, H_q, H_kv, 16, 0, 60, page_size=page_size,
+                                causal=causal, seed=11)
+    inp = workloads.make_extend(case)
+    o, lse = oracle.extend(inp.q, inp.k, inp.v, inp.page_table, inp.kv_lens, causal=causal,
+                           scale=case.scale)
+    ref_o, ref_lse = _extend_torch_ref(inp, causal, case.scale)
+    torch.testing.assert_close(torch.from_numpy(o), ref_o, rtol=0, atol=TOL)
+    torch.testing.assert_close(torch.from_numpy(lse), ref_lse, rtol=0, atol=TOL)
+
+
+def test_extend_brute_force_tiny():
+    """Pure-Python loops over a 2-sequence, 3-query, 8-token-page case."""
+    case = workloads.ExtendCase("t", 2, 3, 2, 1, 4, 0, 6, page_size=8, causal=True, seed=12)
+    inp = workloads.make_extend(case, prefix_lens=[6, 0])
+    scale = 0.7
+    o, lse = oracle.extend(inp.q, inp.k, inp.v, inp.page_table, inp.kv_lens, causal=True,
+                           scale=scale)
+    q = inp.q.double().tolist()
+    k = inp.k.double().tolist()
+    v = inp.v.double().tolist()
+    for b in range(2):
+        n = int(inp.kv_lens[b])
+        for h in range(2):
+            for i in range(3):
+                keys = range(0, i + n - 3 + 1)
+                s = []
+                for j in keys:
+                    pg, sl = int(inp.page_table[b, j // 8]), j % 8
+                    s.append(scale * sum(q[b][i][h][d] * k[pg][sl][0][d] for d in range(4)))
+                w = [math.exp(x) for x in s]
+                tot = sum(w)
+                for d in range(4):
+                    num = sum(w[jj] * v[int(inp.page_table[b, j // 8])][j % 8][0][d]
+                              for jj, j in enumerate(keys))
+                    assert abs(o[b, i, h, d] - num / tot) < 1e-12
+                assert abs(lse[b, h, i] - math.log(tot)) < 1e-12
+
+
+def test_extend_short_cache_and_constant_v():
+    """kv_len < S_q leaves the first rows with no visible key (o = 0, lse =
+    -inf); with V constant per kv head every visible row returns that constant."""
+    case = workloads.ExtendCase("t", 2, 10, 4, 2, 8, 0, 5, page_size=8, causal=True, seed=13)
+    inp = workloads.make_extend(case, prefix_lens=[0, 5])
+    inp.kv_lens[0] = 4  # only 4 cached keys for 10 new queries
+    inp.v[:] = torch.arange(2, dtype=inp.v.dtype).view(1, 1, 2, 1) + 3.0
+    o, lse = oracle.extend(inp.q, inp.k, inp.v, inp.page_table, inp.kv_lens, causal=True,
+                           scale=0.4)
+    assert np.all(o[0, :6] == 0.0) and np.all(np.isneginf(lse[0, :, :6]))
+    assert np.all(np.isfinite(lse[0, :, 6:])) and np.all(np.isfinite(lse[1]))
+    want = np.array([3.0, 3.0, 4.0, 4.0]).reshape(1, 4, 1)  # heads 0,1 -> kv 0; 2,3 -> kv 1
+    np.testing.assert_allclose(o[0, 6:], np.broadcast_to(want, (4, 4, 8)), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(o[1], np.broadcast_to(want, (10, 4, 8)), rtol=0, atol=1e-12)
+
+
+def test_extend_without_prefix_equals_causal_prefill():
+    """With no cached prefix and identity-free random pages, extend is the
+    square causal prefill of the gathered sequence (BSHD)."""
+    case = workloads.ExtendCase("t", 2, 37, 4, 4, 16, 0, 0, page_size=16, causal=True, seed=14)
+    inp = workloads.make_extend(case)
+    o, lse = oracle.extend(inp.q, inp.k, inp.v, inp.page_table, inp.kv_lens, causal=True,
+                           scale=0.25)
+    for b in range(2):
+        t = torch.arange(37)
+        phys = inp.page_table[b].long()[t // 16]
+        kb, vb = inp.k[phys, t % 16][None], inp.v[phys, t % 16][None]
+        po, plse = oracle.prefill(inp.q[b:b + 1], kb, vb, causal=True, scale=0.25,
+                                  layout=oracle.BSHD)
+        np.testing.assert_allclose(o[b], po[0], rtol=0, atol=TOL)
+        np.testing.assert_allclose(lse[b], plse[0], rtol=0, atol=TOL)
+
+
 # --------------------------------------------------------- planted mistakes
 
 _MUTANTS = {
     "causal_off_by_one": ("long lim = i + (J->S_kv - J->S_q);",
                           "long lim = i + (J->S_kv - J->S_q) - 1;"),
     "causal_top_left": ("long lim = i + (J->S_kv - J->S_q);", "long lim = i;"),
-    "dropped_scale": ("s_buf[j] = J->scale * dot;", "s_buf[j] = dot;"),
+    "dropped_scale": ("k_row[d];\n        s_buf[j] = J->scale * dot;",
+                      "k_row[d];\n        s_buf[j] = dot;"),
+    "extend_dropped_scale": ("k_seq[j * D + d];\n                s_buf[j] = J->scale * dot;",
+                             "k_seq[j * D + d];\n                s_buf[j] = dot;"),
     "lse_without_max": ("*lse_out = m + log(l);\n}", "*lse_out = log(l);\n}"),
     "bshd_as_bhsd": ("return (size_t)(((b * S + s) * H + h) * D + d);",
                      "return (size_t)(((b * H + h) * S + s) * D + d);"),
     "gqa_modulo": ("g = h / group;", "g = h % J->H_kv;"),
-    "page_slot": ("long slot = t % J->page_size;", "long slot = t / J->page_size;"),
+    "page_slot": ("long slot = t % page_size;", "long slot = t / page_size;"),
+    "extend_causal_top_left": ("long lim = i + (kv_len - J->S_q);", "long lim = i;"),
+    "extend_gqa_modulo": ("kvh = h / group;", "kvh = h % J->H_kv;"),
+    "extend_q_as_bhsd": ("J->q + (size_t)(((b * J->S_q + i) * J->H_q + h) * D)",
+                         "J->q + (size_t)(((b * J->H_q + h) * J->S_q + i) * D)"),
+    "extend_lse_index": ("J->lse + (size_t)((b * J->H_q + h) * J->S_q + i)",
+                         "J->lse + (size_t)((b * J->S_q + i) * J->H_q + h)"),
     "v_from_k": ("o_row[d] += w * v_seq[t * D + d];", "o_row[d] += w * k_seq[t * D + d];"),
 }
 
@@ -302,6 +414,7 @@ def _pins_pass() -> bool:
         lambda: test_prefill_matches_torch_sdpa(1, 2, 33, 70, 64, True, "bshd"),
         lambda: test_prefill_matches_torch_sdpa(2, 1, 64, 64, 128, False, "bhsd"),
         lambda: test_decode_matches_torch_sdpa(True, 8, 2),
+        lambda: test_extend_matches_torch_sdpa(True, 8, 2, 8),
     ] + [lambda p=p: test_golden_fixture(p)
          for p in sorted(glob.glob(os.path.join(GOLDEN, "*.json")))]
     for c in checks:
@@ -333,6 +446,8 @@ def test_mutants_are_caught(name):
         mutant.oracle_prefill_f64.restype = ctypes.c_int
         mutant.oracle_decode_f64.argtypes = saved.oracle_decode_f64.argtypes
         mutant.oracle_decode_f64.restype = ctypes.c_int
+        mutant.oracle_extend_f64.argtypes = saved.oracle_extend_f64.argtypes
+        mutant.oracle_extend_f64.restype = ctypes.c_int
         oracle._lib = mutant
         try:
             assert not _pins_pass(), "pins did not catch planted mistake %r" % name

@@ -19,6 +19,11 @@ Recipe (every draw uses a CPU ``torch.Generator`` seeded with ``seed``):
   data pages placed by the permutation, one extra poison page (all 1e4) is
   appended, unused page-table entries point at it, and page tail slots hold
   1e4 too, so a masking bug is loud but never reads outside the pool.
+* extend (prefill of new tokens against a paged cache): first the cached
+  prefix lengths (``randint`` uniform on [prefix_min, prefix_max]) unless
+  given, ``kv_len_b = prefix_b + S_q``; then Q [B,S_q,H_q,D]; then per
+  sequence its K rows then V rows; then the page permutation, poison page and
+  poison tails exactly as for paged decode.
 
 The five named workloads follow the configurations this library is measured
 on; their shapes mirror the pages' LLM attention workloads (e.g. the
@@ -89,6 +94,33 @@ class DecodeCase:
         return -(-self.S_max // self.page_size)
 
 
+@dataclass(frozen=True)
+class ExtendCase:
+    """S_q new query tokens per sequence against ``prefix + S_q`` cached keys
+    in a paged pool (bottom-right causal per sequence when ``causal``)."""
+    name: str
+    B: int
+    S_q: int
+    H_q: int
+    H_kv: int
+    D: int
+    prefix_min: int
+    prefix_max: int
+    page_size: int = 16
+    dtype: str = "bf16"
+    causal: bool = True
+    std: float = 1.0
+    seed: int = 0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+    @property
+    def max_pages(self) -> int:
+        return -(-(self.prefix_max + self.S_q) // self.page_size)
+
+
 def visible_pairs(S_q: int, S_kv: int, causal: bool) -> int:
     """Number of (query, key) pairs the mask leaves visible (bottom-right causal)."""
     if not causal:
@@ -112,6 +144,12 @@ C4 = DecodeCase("decode_contig_bf16_b32_hq32_hkv8_d128", 32, 32, 8, 128, 1024, 3
                 paged=False)
 C5 = DecodeCase("decode_paged16_bf16_b32_hq32_hkv8_d128", 32, 32, 8, 128, 1, 32768, 32768,
                 paged=True)
+
+
+# Prefix-cached prefill: 8 requests of 1024 new tokens each on top of cached
+# prefixes of up to 15360 tokens, Llama-3-8B-like GQA heads, 16-token pages.
+C6 = ExtendCase("extend_paged16_bf16_b8_sq1024_hq32_hkv8_d128_causal", 8, 1024, 32, 8, 128, 0,
+                15360)
 
 
 def _gen(seed: int) -> torch.Generator:
@@ -184,23 +222,8 @@ def make_decode(case: DecodeCase, kv_lens=None) -> DecodeInputs:
             v[b, :n] = rows_v[b]
         return DecodeInputs(q, k, v, lens32, None, case.S_max, 1)
     ps = case.page_size
-    pages_per_seq = [-(-int(n) // ps) for n in kv_lens.tolist()]
-    n_data = sum(pages_per_seq)
-    perm = torch.randperm(n_data, generator=g)
-    poison_page = n_data
-    k = torch.full((n_data + 1, ps, case.H_kv, case.D), POISON, dtype=dt)
-    v = torch.full((n_data + 1, ps, case.H_kv, case.D), POISON, dtype=dt)
-    page_table = torch.full((case.B, case.max_pages), poison_page, dtype=torch.int32)
-    cursor = 0
-    for b in range(case.B):
-        n = int(kv_lens[b])
-        for p in range(pages_per_seq[b]):
-            phys = int(perm[cursor])
-            cursor += 1
-            page_table[b, p] = phys
-            lo, hi = p * ps, min(n, (p + 1) * ps)
-            k[phys, : hi - lo] = rows_k[b][lo:hi]
-            v[phys, : hi - lo] = rows_v[b][lo:hi]
+    k, v, page_table = _place_pages(g, rows_k, rows_v, kv_lens, ps, case.max_pages, case.H_kv,
+                                    case.D, dt)
     return DecodeInputs(q, k, v, lens32, page_table, ps, case.max_pages)
 
 
@@ -224,3 +247,68 @@ def contiguous_view_of(inp: DecodeInputs, S_max: int | None = None) -> DecodeInp
             k[b, lo:hi] = inp.k[phys, : hi - lo]
             v[b, lo:hi] = inp.v[phys, : hi - lo]
     return DecodeInputs(inp.q, k, v, inp.kv_lens, None, S_max, 1)
+
+
+@dataclass
+class ExtendInputs:
+    q: torch.Tensor  # [B, S_q, H_q, D]
+    k: torch.Tensor  # pool [num_pages, page_size, H_kv, D]
+    v: torch.Tensor
+    kv_lens: torch.Tensor  # [B] int32, prefix + S_q
+    page_table: torch.Tensor  # [B, max_pages] int32
+    page_size: int
+    max_pages: int
+
+    def visible_pairs(self, causal: bool) -> int:
+        S_q = self.q.shape[1]
+        return sum(visible_pairs(S_q, int(n), causal) for n in self.kv_lens.tolist())
+
+    def flops(self, causal: bool) -> float:
+        """Algorithmic FLOPs: 4*D per visible (query, key) pair and query head."""
+        H_q, D = self.q.shape[2], self.q.shape[3]
+        return 4.0 * H_q * D * self.visible_pairs(causal)
+
+
+def _place_pages(g, rows_k, rows_v, kv_lens, ps, max_pages, H_kv, D, dt):
+    """Scatter per-sequence rows into a permuted page pool (shared by paged
+    decode and extend): returns (k_pool, v_pool, page_table)."""
+    B = len(rows_k)
+    pages_per_seq = [-(-int(n) // ps) for n in kv_lens.tolist()]
+    n_data = sum(pages_per_seq)
+    perm = torch.randperm(n_data, generator=g)
+    poison_page = n_data
+    k = torch.full((n_data + 1, ps, H_kv, D), POISON, dtype=dt)
+    v = torch.full((n_data + 1, ps, H_kv, D), POISON, dtype=dt)
+    page_table = torch.full((B, max_pages), poison_page, dtype=torch.int32)
+    cursor = 0
+    for b in range(B):
+        n = int(kv_lens[b])
+        for p in range(pages_per_seq[b]):
+            phys = int(perm[cursor])
+            cursor += 1
+            page_table[b, p] = phys
+            lo, hi = p * ps, min(n, (p + 1) * ps)
+            k[phys, : hi - lo] = rows_k[b][lo:hi]
+            v[phys, : hi - lo] = rows_v[b][lo:hi]
+    return k, v, page_table
+
+
+def make_extend(case: ExtendCase, prefix_lens=None) -> ExtendInputs:
+    """Return CPU tensors for an extend case (see the module docstring recipe)."""
+    g = _gen(case.seed)
+    dt = _DTYPES[case.dtype]
+    if prefix_lens is None:
+        prefix_lens = torch.randint(case.prefix_min, case.prefix_max + 1, (case.B,), generator=g,
+                                    dtype=torch.int64)
+    prefix_lens = torch.as_tensor(prefix_lens, dtype=torch.int64)
+    assert int(prefix_lens.min()) >= 0 and int(prefix_lens.max()) <= case.prefix_max
+    kv_lens = prefix_lens + case.S_q
+    q = _randn(g, (case.B, case.S_q, case.H_q, case.D), case.std, dt)
+    rows_k, rows_v = [], []
+    for b in range(case.B):
+        n = int(kv_lens[b])
+        rows_k.append(_randn(g, (n, case.H_kv, case.D), case.std, dt))
+        rows_v.append(_randn(g, (n, case.H_kv, case.D), case.std, dt))
+    k, v, pt = _place_pages(g, rows_k, rows_v, kv_lens, case.page_size, case.max_pages,
+                            case.H_kv, case.D, dt)
+    return ExtendInputs(q, k, v, kv_lens.to(torch.int32), pt, case.page_size, case.max_pages)
