@@ -43,7 +43,8 @@ _STATUS_NAMES = {
 }
 
 # Names the header exports (checked against include/attn_gb300.h by the tests).
-EXPORTED = ("attn_prefill_fwd", "attn_decode_fwd", "attn_decode_fwd_noalloc", "attn_last_error",
+EXPORTED = ("attn_prefill_fwd", "attn_extend_fwd", "attn_decode_fwd", "attn_decode_fwd_noalloc",
+            "attn_last_error",
             "attn_device_error", "attn_set_wait_limit_ns", "attn_release_workspace",
             "attn_version")
 
@@ -76,6 +77,9 @@ def lib() -> ctypes.CDLL:
             L.attn_prefill_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, cf,
                                            vp]
             L.attn_prefill_fwd.restype = ci
+            L.attn_extend_fwd.argtypes = [vp, vp, vp, i32p, i32p, vp, vp, ci, ci, ci, ci, ci, ci,
+                                          ci, ci, ci, ci, cf, vp]
+            L.attn_extend_fwd.restype = ci
             L.attn_decode_fwd.argtypes = [vp, vp, vp, i32p, i32p, vp, ci, ci, ci, ci, ci, ci, ci,
                                           ci, cf, ci, vp]
             L.attn_decode_fwd.restype = ci
@@ -113,6 +117,15 @@ def attn_prefill_fwd(q, k, v, o, lse, B, H, S_q, S_kv, D, layout, dtype, causal,
     """C ``attn_prefill_fwd``; pointers and stream as ints.  Returns the status."""
     return lib().attn_prefill_fwd(q, k, v, o, lse, B, H, S_q, S_kv, D, layout, dtype, causal,
                                   scale, stream)
+
+
+def attn_extend_fwd(q, k_pool, v_pool, page_table, kv_lens, o, lse, B, S_q, H_q, H_kv, D,
+                    page_size, max_pages_per_seq, num_pages, dtype, causal, scale,
+                    stream) -> int:
+    """C ``attn_extend_fwd``; pointers and stream as ints.  Returns the status."""
+    return lib().attn_extend_fwd(q, k_pool, v_pool, page_table, kv_lens, o, lse, B, S_q, H_q,
+                                 H_kv, D, page_size, max_pages_per_seq, num_pages, dtype, causal,
+                                 scale, stream)
 
 
 def attn_decode_fwd(q, k_pool, v_pool, page_table, kv_lens, o, B, H_q, H_kv, D, page_size,
@@ -222,6 +235,41 @@ def prefill(q, k, v, *, causal: bool = False, scale: float | None = None,
     return (out, lse) if return_lse else out
 
 
+def extend(q, k_pool, v_pool, page_table, kv_lens, *, causal: bool = True,
+           scale: float | None = None, num_pages: int | None = None, out=None, lse=None,
+           return_lse: bool = False, stream=None):
+    """Extend (prefix-cached prefill) over torch CUDA tensors.
+
+    ``q`` [B,S_q,H_q,D]; ``k_pool``/``v_pool`` [num_pages, page_size, H_kv, D];
+    ``page_table`` [B, max_pages] int32; ``kv_lens`` [B] int32 = cached prefix
+    plus the S_q new tokens (already written to the pool).  Returns ``o``
+    [B,S_q,H_q,D] (and ``lse`` [B,H_q,S_q] fp32 if requested).
+    """
+    torch = _torch()
+    _require_cuda(q, k_pool, v_pool, kv_lens, page_table, out, lse)
+    B, S_q, H_q, D = q.shape
+    n_pages, page_size, H_kv, D2 = k_pool.shape
+    if D2 != D or v_pool.shape != k_pool.shape:
+        raise ValueError("k_pool/v_pool must be [pages, page_size, H_kv, D]")
+    if k_pool.dtype != q.dtype or v_pool.dtype != q.dtype:
+        raise ValueError("k_pool and v_pool must have q's dtype")
+    if kv_lens.dtype != torch.int32 or page_table.dtype != torch.int32:
+        raise TypeError("kv_lens and page_table must be int32")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if return_lse and lse is None:
+        lse = torch.empty((B, H_q, S_q), device=q.device, dtype=torch.float32)
+    _check(attn_extend_fwd(q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(),
+                           page_table.data_ptr(), kv_lens.data_ptr(), out.data_ptr(),
+                           lse.data_ptr() if lse is not None else None, B, S_q, H_q, H_kv, D,
+                           page_size, page_table.shape[1],
+                           n_pages if num_pages is None else num_pages, _dtype_code(q),
+                           int(bool(causal)), float(scale), _stream_handle(stream)))
+    return (out, lse) if return_lse else out
+
+
 def decode(q, k_pool, v_pool, kv_lens, *, page_table=None, num_pages: int | None = None,
            num_splits: int = 0, scale: float | None = None, out=None, stream=None):
     """Decode attention over torch CUDA tensors.
@@ -265,4 +313,4 @@ def check_device_error() -> None:
 
 
 __all__ = [n for n in dir() if n.startswith(("attn_", "ATTN_"))] + [
-    "AttnError", "prefill", "decode", "lib", "library_path", "check_device_error", "EXPORTED"]
+    "AttnError", "prefill", "extend", "decode", "lib", "library_path", "check_device_error", "EXPORTED"]

@@ -219,6 +219,81 @@ attn_status attn_prefill_fwd(const void* q, const void* k, const void* v, void* 
   return ATTN_OK;
 }
 
+attn_status attn_extend_fwd(const void* q, const void* k_pool, const void* v_pool,
+                            const int32_t* page_table, const int32_t* kv_lens, void* o, float* lse,
+                            int B, int S_q, int H_q, int H_kv, int D, int page_size,
+                            int max_pages_per_seq, int num_pages, attn_dtype dtype, int causal,
+                            float scale, cudaStream_t stream) {
+  if (B < 0 || S_q < 0) return fail(ATTN_ERR_INVALID_ARG, "B and S_q must be >= 0");
+  if (H_q <= 0 || H_kv <= 0) return fail(ATTN_ERR_INVALID_ARG, "H_q and H_kv must be > 0");
+  if (H_q % H_kv != 0) return fail(ATTN_ERR_INVALID_ARG, "H_q must be a multiple of H_kv");
+  if (D != 64 && D != 128) return fail(ATTN_ERR_UNSUPPORTED, "D must be 64 or 128");
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16)
+    return fail(ATTN_ERR_INVALID_ARG, "dtype must be ATTN_F16 or ATTN_BF16");
+  if (causal != 0 && causal != 1) return fail(ATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (!(std::isfinite(scale) && scale > 0.f))
+    return fail(ATTN_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (page_size <= 0 || max_pages_per_seq <= 0 || num_pages <= 0)
+    return fail(ATTN_ERR_INVALID_ARG, "page_size, max_pages_per_seq and num_pages must be > 0");
+  const int tile = attn_sm103a::prefill_box_rows();
+  const bool small_ok = page_size >= 8 && page_size <= tile && tile % page_size == 0;
+  if (!small_ok && page_size % tile != 0)
+    return fail(ATTN_ERR_UNSUPPORTED, "page_size must be 8, 16, 32, 64 or a multiple of 128");
+  if (static_cast<int64_t>(B) * S_q == 0) return ATTN_OK;  // nothing to compute
+  if (!q || !k_pool || !v_pool || !page_table || !kv_lens || !o)
+    return fail(ATTN_ERR_INVALID_ARG,
+                "q, k_pool, v_pool, page_table, kv_lens and o must be non-NULL");
+  if (!aligned16(q) || !aligned16(o) || !aligned16(k_pool) || !aligned16(v_pool))
+    return fail(ATTN_ERR_INVALID_ARG, "q, k_pool, v_pool and o must be 16-byte aligned");
+  if (static_cast<int64_t>(max_pages_per_seq) * page_size > 0x7FFFFFFF)
+    return fail(ATTN_ERR_UNSUPPORTED, "KV capacity exceeds 2^31 keys");
+  if (static_cast<int64_t>(num_pages) * page_size * H_kv * D * 2 >= (int64_t(1) << 40) ||
+      static_cast<int64_t>(B) * S_q * H_q * D * 2 >= (int64_t(1) << 40))
+    return fail(ATTN_ERR_UNSUPPORTED, "tensor too large for one TMA descriptor");
+  const int rows = attn_sm103a::prefill_rows_per_cta();
+  const int64_t n_qb = (S_q + rows - 1) / rows;
+  if (static_cast<int64_t>(B) * H_q * n_qb > 0x7FFFFFFF)
+    return fail(ATTN_ERR_UNSUPPORTED, "grid too large");
+
+  DeviceState* st = nullptr;
+  attn_status s = device_state(&st);
+  if (s != ATTN_OK) return s;
+
+  const bool bf16 = dtype == ATTN_BF16;
+  const int box_rows = page_size < tile ? page_size : tile;
+  CUtensorMap mq, mk, mv, mo;
+  if (!prefill_map(&mq, q, B, H_q, S_q, D, true, bf16) ||
+      !prefill_map(&mo, o, B, H_q, S_q, D, true, bf16) ||
+      !decode_map(&mk, k_pool, num_pages, page_size, H_kv, D, box_rows, bf16) ||
+      !decode_map(&mv, v_pool, num_pages, page_size, H_kv, D, box_rows, bf16))
+    return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed for an extend tensor");
+
+  attn_sm103a::PrefillParams p{};
+  p.lse = lse;
+  p.B = B;
+  p.H = H_q;
+  p.S_q = S_q;
+  p.S_kv = 0;  // per sequence, from kv_lens
+  p.num_q_blocks = static_cast<int>(n_qb);
+  p.causal = causal;
+  p.bshd = 1;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.err = st->err_word;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  p.page_table = page_table;
+  p.kv_lens = kv_lens;
+  p.max_pages = max_pages_per_seq;
+  p.page_size = page_size;
+  p.num_pages = num_pages;
+  p.group = H_q / H_kv;
+  p.H_kv = H_kv;
+  p.k_pool = k_pool;
+  p.v_pool = v_pool;
+  cudaError_t e = attn_sm103a::extend_launch(mq, mk, mv, mo, p, D, bf16, stream);
+  if (e != cudaSuccess) return fail_cuda(e, "extend launch");
+  return ATTN_OK;
+}
+
 attn_status attn_decode_fwd(const void* q, const void* k_pool, const void* v_pool,
                             const int32_t* page_table, const int32_t* kv_lens, void* o, int B,
                             int H_q, int H_kv, int D, int page_size, int max_pages_per_seq,

@@ -29,6 +29,13 @@
 // Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D),
 // O1 [256+D, 256+2D).  P_t (16-bit pairs) overwrites the first 64 columns of
 // S_t.
+//
+// The extend form (new tokens of a sequence against its cached keys, Wave
+// February 2025 Release, "Extend Attention"; WAVE MLSys 2026 summary,
+// Integration: SGLang extend) is the same kernel with kPaged: the whole TMA
+// warp gathers each 128-key K/V tile page by page through the page table
+// (one lane per page-sized box), the key count and the causal diagonal come
+// from the sequence's kv_len, and query head h reads kv head h / group.
 #include "prefill_sm103a.h"
 #include "sm103a_ptx.cuh"
 
@@ -71,9 +78,11 @@ struct SharedCtl {
   uint64_t tmem_free;  // every softmax warp is done reading tensor memory
   uint64_t kv_full[10];
   uint64_t kv_empty[10];
+  uint64_t tail_v;     // extend form: the V tile holding the sequence end has landed
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(SharedCtl) <= 256, "control block must fit its reserved bytes");
 
 // TMA load of one 64-column box of rows [row, row + 128) of (batch b, head h).
 // BHSD maps are (D, S, H, B); BSHD maps are (D, H, S, B).
@@ -100,16 +109,151 @@ __device__ __forceinline__ void prefetch_box(const CUtensorMap* map, int x, int 
 constexpr int kL2PrefetchTiles = 4;
 
 // Number of KV tiles a query tile [row0, row0 + kBM) must visit.
-__device__ __forceinline__ int kv_tiles_for(int row0, const PrefillParams& p) {
-  int keys = p.S_kv;
+__device__ __forceinline__ int kv_tiles_for(int row0, int S_kv, const PrefillParams& p) {
+  int keys = S_kv;
   if (p.causal) {
     int last_row = min(row0 + kBM, p.S_q) - 1;
-    keys = min(keys, last_row + (p.S_kv - p.S_q) + 1);
+    keys = min(keys, last_row + (S_kv - p.S_q) + 1);
   }
   return keys <= 0 ? 0 : (keys + kBN - 1) / kBN;
 }
 
-template <int D, bool kBF16>
+// Producer of the extend form: the whole warp streams K/V tiles gathered
+// through the page table.  Lane (bx, half) owns box bx (one page, or 128 rows
+// of a larger page) of 64-column half `half` of each tile.  Keys past the
+// sequence end are never multiplied by a nonzero weight, but their V rows
+// may hold anything (0 * NaN = NaN), so the V tile holding the sequence end
+// lands on its own barrier, the warp zeroes rows [valid, 128) and only then
+// publishes the stage.
+template <int D>
+__device__ __forceinline__ void produce_paged(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                                              const CUtensorMap& tm_v, const PrefillParams& p,
+                                              SharedCtl* ctl, uint8_t* s_q, uint8_t* s_kv, int b,
+                                              int h, int S_kv, int row_base, int n_all,
+                                              int lane) {
+  using C = Cfg<D>;
+  constexpr int kHalves = D / 64;
+  constexpr uint32_t kAll = 0xffffffffu;
+  const int g = h / p.group;
+  const int ps = p.page_size;
+  const int box_rows = min(ps, kBN);
+  const int half = lane % kHalves;
+  const int bx = lane / kHalves;
+  const int32_t* pt = p.page_table + static_cast<size_t>(b) * p.max_pages;
+  // Page and slot of this lane's box in KV tile j: 0 if the box holds no key,
+  // 1 for a valid page, 2 for a page id outside the pool (flagged; the load
+  // then starts past the pool's end and the TMA fills the box with zeros).
+  auto locate = [&](int j, int& page, int& slot) {
+    const int key = j * kBN + bx * box_rows;
+    if (bx * box_rows >= kBN || key >= S_kv) return 0;
+    page = __ldg(pt + key / ps);
+    slot = key % ps;
+    if (page < 0 || page >= p.num_pages) {
+      record_error(p.err, kErrBadArgument, 4);
+      page = p.num_pages;
+      return 2;
+    }
+    return 1;
+  };
+  volatile int* abort_flag = &ctl->abort;
+  if (lane == 0) {
+    tma_prefetch_map(&tm_q);
+    tma_prefetch_map(&tm_k);
+    tma_prefetch_map(&tm_v);
+    for (int t = 0; t < kTiles; ++t) {
+      mbar_arrive_expect_tx(&ctl->q_full[t], C::kTileBytes);
+      for (int x = 0; x < kHalves; ++x)
+        tma_load_4d(s_q + t * C::kTileBytes + x * (kBM * 128), &tm_q, &ctl->q_full[t], x * 64, h,
+                    row_base + t * kBM, b);
+    }
+  }
+  for (int j = 0; j < min(n_all, kL2PrefetchTiles); ++j) {
+    int pg, sl;
+    if (locate(j, pg, sl) == 1) {
+      tma_prefetch_l2_4d(&tm_k, half * 64, g, sl, pg);
+      tma_prefetch_l2_4d(&tm_v, half * 64, g, sl, pg);
+    }
+  }
+  int issued = 0, tail_idx = -1;
+  for (int j = 0; j < n_all; ++j) {
+    if (__shfl_sync(kAll, *abort_flag, 0)) break;
+    if (j + kL2PrefetchTiles < n_all) {
+      int pg, sl;
+      if (locate(j + kL2PrefetchTiles, pg, sl) == 1) {
+        tma_prefetch_l2_4d(&tm_k, half * 64, g, sl, pg);
+        tma_prefetch_l2_4d(&tm_v, half * 64, g, sl, pg);
+      }
+    }
+    int pg = 0, sl = 0;
+    const bool mine = locate(j, pg, sl) != 0;
+    const int valid = min(kBN, S_kv - j * kBN);  // keys of this tile inside the sequence
+    const int n_box = (valid + box_rows - 1) / box_rows;
+    const uint32_t bytes = static_cast<uint32_t>(n_box * box_rows * 128 * kHalves);
+    bool ok = true;
+#pragma unroll 1
+    for (int kind = 0; kind < 2 && ok; ++kind) {
+      const int idx = 2 * j + kind;
+      const int st = idx % C::kStages;
+      const int round = idx / C::kStages;
+      if (round > 0) {
+        bool w = true;
+        if (lane == 0) w = mbar_wait(&ctl->kv_empty[st], (round - 1) & 1, p.wait_limit_ns, p.err, 13);
+        if (!(ok = __shfl_sync(kAll, w, 0))) break;
+      }
+      uint8_t* dst = s_kv + st * C::kTileBytes;
+      const bool fix_v = kind == 1 && valid < kBN;
+      uint64_t* bar = fix_v ? &ctl->tail_v : &ctl->kv_full[st];
+      if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
+      __syncwarp();
+      if (mine)
+        tma_load_4d(dst + half * (kBN * 128) + bx * box_rows * 128, kind ? &tm_v : &tm_k, bar,
+                    half * 64, g, sl, pg);
+      issued = idx + 1;
+      if (fix_v) {
+        tail_idx = idx;
+        if (!(ok = __all_sync(kAll, mbar_wait(&ctl->tail_v, 0, p.wait_limit_ns, p.err, 14))))
+          break;
+        const int chunks = (kBN - valid) * 8;  // 16-byte chunks past the end, per half
+        for (int c = lane; c < chunks * kHalves; c += 32) {
+          const int hh = c / chunks, rem = c % chunks;
+          *reinterpret_cast<uint4*>(dst + hh * (kBN * 128) + (valid + rem / 8) * 128 +
+                                    (rem % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();  // the zeros must be visible to the tensor core
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->kv_full[st]);
+      }
+    }
+    if (!ok) {
+      if (lane == 0) *abort_flag = 1;
+      break;
+    }
+  }
+  // Never leave the CTA with a copy still landing in shared memory.
+  if (lane == 0) {
+    for (int idx = max(0, issued - C::kStages); idx < issued; ++idx)
+      if (idx == tail_idx)
+        mbar_wait(&ctl->tail_v, 0, p.wait_limit_ns, p.err, 15);
+      else
+        mbar_wait(&ctl->kv_full[idx % C::kStages], (idx / C::kStages) & 1, p.wait_limit_ns,
+                  p.err, 11);
+    for (int t = 0; t < kTiles; ++t) mbar_wait(&ctl->q_full[t], 0, p.wait_limit_ns, p.err, 12);
+  }
+}
+
+// Keys of sequence b in the extend form: kv_lens[b], clamped to the page
+// table's capacity (a value outside [0, capacity] is flagged).
+__device__ __forceinline__ int extend_kv_len(int b, const PrefillParams& p) {
+  const int cap = p.max_pages * p.page_size;
+  int kv = p.kv_lens[b];
+  if (kv < 0 || kv > cap) {
+    if (threadIdx.x == 0) record_error(p.err, kErrBadArgument, 3);
+    kv = kv < 0 ? 0 : cap;
+  }
+  return kv;
+}
+
+template <int D, bool kBF16, bool kPaged>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -133,9 +277,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int qb = nqb - 1 - (blockIdx.x % nqb);
   const int b = bh / p.H;
   const int h = bh % p.H;
+  const int S_kv = kPaged ? extend_kv_len(b, p) : p.S_kv;  // keys of this sequence
   const int row_base = qb * (kTiles * kBM);
-  const int n_kv0 = kv_tiles_for(row_base, p);
-  const int n_kv1 = kv_tiles_for(row_base + kBM, p);
+  const int n_kv0 = kv_tiles_for(row_base, S_kv, p);
+  const int n_kv1 = kv_tiles_for(row_base + kBM, S_kv, p);
   auto n_kv = [&](int t) { return t == 0 ? n_kv0 : n_kv1; };  // KV tiles of query tile t
   const int n_all = max(n_kv0, n_kv1);  // tile 1 never needs fewer than tile 0
 
@@ -152,6 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&ctl->o_full, 1);
     mbar_init(&ctl->tmem_free, 8);
+    mbar_init(&ctl->tail_v, 1);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&ctl->kv_full[s], 1);
       mbar_init(&ctl->kv_empty[s], 1);
@@ -167,7 +313,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp >= 8) {
    // ============================================= control warpgroup
    setmaxnreg_dec<kRegsControl>();
-   if (warp == kWarpTma) {
+   if (kPaged && warp == kWarpTma) {
+    // ------------------------------------------------- producer (paged K/V)
+    if (n_all > 0) produce_paged<D>(tm_q, tm_k, tm_v, p, ctl, s_q, s_kv, b, h, S_kv, row_base,
+                                    n_all, lane);
+    __syncwarp();
+   } else if (warp == kWarpTma) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && n_all > 0) {
       int issued = 0;  // KV loads issued so far
@@ -327,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = wl * 32 + lane;       // row within the tile
     const int row0 = row_base + t * kBM;
     const int i = row0 + r;             // query index
-    const int diag = p.S_kv - p.S_q;    // bottom-right causal offset
+    const int diag = S_kv - p.S_q;      // bottom-right causal offset
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wl * 32) << 16);
     const uint32_t col_s = C::col_s(t);
     const uint32_t col_o = C::col_o(t);
@@ -344,9 +495,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       float s[kBN];
       tmem_ld128_wait(lane_addr + col_s, s);
       const int key0 = j * kBN;
-      const bool full = (key0 + kBN <= p.S_kv) && (!p.causal || key0 + kBN - 1 <= row0 + diag);
+      const bool full = (key0 + kBN <= S_kv) && (!p.causal || key0 + kBN - 1 <= row0 + diag);
       if (!full) {
-        const int lim = p.causal ? min(p.S_kv - 1, i + diag) : p.S_kv - 1;
+        const int lim = p.causal ? min(S_kv - 1, i + diag) : S_kv - 1;
 #pragma unroll
         for (int cc = 0; cc < kBN; ++cc)
           if (key0 + cc > lim) s[cc] = -INFINITY;
@@ -466,11 +617,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-template <int D, bool kBF16>
+template <int D, bool kBF16, bool kPaged>
 static cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                               const CUtensorMap& o, const PrefillParams& p, int grid,
                               cudaStream_t stream) {
-  auto kern = prefill_fwd_kernel<D, kBF16>;
+  auto kern = prefill_fwd_kernel<D, kBF16, kPaged>;
   static bool configured = false;  // per template instance
   if (!configured) {
     // The in-kernel register split assumes exactly kRegsAtLaunch registers
@@ -493,10 +644,21 @@ cudaError_t prefill_launch(const CUtensorMap& q, const CUtensorMap& k, const CUt
                            cudaStream_t stream) {
   const int grid = p.B * p.H * p.num_q_blocks;
   if (grid == 0) return cudaSuccess;
-  if (D == 128) return bf16 ? launch_one<128, true>(q, k, v, o, p, grid, stream)
-                            : launch_one<128, false>(q, k, v, o, p, grid, stream);
-  return bf16 ? launch_one<64, true>(q, k, v, o, p, grid, stream)
-              : launch_one<64, false>(q, k, v, o, p, grid, stream);
+  if (D == 128) return bf16 ? launch_one<128, true, false>(q, k, v, o, p, grid, stream)
+                            : launch_one<128, false, false>(q, k, v, o, p, grid, stream);
+  return bf16 ? launch_one<64, true, false>(q, k, v, o, p, grid, stream)
+              : launch_one<64, false, false>(q, k, v, o, p, grid, stream);
+}
+
+cudaError_t extend_launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                          const CUtensorMap& o, const PrefillParams& p, int D, bool bf16,
+                          cudaStream_t stream) {
+  const int grid = p.B * p.H * p.num_q_blocks;
+  if (grid == 0) return cudaSuccess;
+  if (D == 128) return bf16 ? launch_one<128, true, true>(q, k, v, o, p, grid, stream)
+                            : launch_one<128, false, true>(q, k, v, o, p, grid, stream);
+  return bf16 ? launch_one<64, true, true>(q, k, v, o, p, grid, stream)
+              : launch_one<64, false, true>(q, k, v, o, p, grid, stream);
 }
 
 int prefill_rows_per_cta() { return kTiles * kBM; }

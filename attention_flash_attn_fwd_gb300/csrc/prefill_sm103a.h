@@ -17,6 +17,14 @@ struct PrefillParams {
   float scale_log2;       // softmax scale * log2(e)
   int* err;               // device error word
   uint64_t wait_limit_ns; // bound on every mbarrier wait
+  // Paged K/V (extend form only; unused by the contiguous prefill):
+  const int32_t* page_table;  // [B, max_pages] physical page ids
+  const int32_t* kv_lens;     // [B] keys per sequence (S_kv is ignored)
+  int max_pages, page_size, num_pages;
+  int group;                  // query heads per kv head (H / H_kv)
+  int H_kv;
+  const void* k_pool;         // [num_pages, page_size, H_kv, D]
+  const void* v_pool;
 };
 
 // Tensor maps: 16-bit elements, 128-byte swizzle, box = 64 columns x
@@ -24,6 +32,13 @@ struct PrefillParams {
 cudaError_t prefill_launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                            const CUtensorMap& o, const PrefillParams& p, int D, bool bf16,
                            cudaStream_t stream);
+
+// Extend form: q/o maps as BSHD (D, H, S_q, B); k/v maps over the pool
+// [num_pages, page_size, H_kv, D] as (D, H_kv, page_size, num_pages) with box
+// (64, 1, min(page_size, 128), 1).
+cudaError_t extend_launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                          const CUtensorMap& o, const PrefillParams& p, int D, bool bf16,
+                          cudaStream_t stream);
 
 int prefill_rows_per_cta();
 int prefill_box_rows();

@@ -83,6 +83,43 @@ ATTN_API attn_status attn_prefill_fwd(const void* q, const void* k, const void* 
                              attn_dtype dtype, int causal, float scale, cudaStream_t stream);
 
 /*
+ * Extend attention forward: prefill of S_q new tokens per sequence against the
+ * sequence's cached keys in a paged KV pool (prefix-cached / chunked prefill).
+ *
+ * Defines: O[b,i,h,:] = sum_t softmax_t(scale * q[b,i,h] . k_t) v_t over the
+ * keys t < kv_lens[b] of sequence b visible to query i, read from kv head
+ * g = h / (H_q / H_kv) ("Extend Attention", Wave February 2025 Release; the
+ * SGLang extend mode, WAVE MLSys 2026 summary, Integration).  kv_lens[b]
+ * counts the cached prefix AND the S_q new tokens, whose K/V the caller has
+ * already written to the pool; with causal, key t is visible to query i iff
+ * t <= i + (kv_lens[b] - S_q) (bottom-right, per sequence).
+ *
+ *   q          [B,S_q,H_q,D] dtype (BSHD)
+ *   k_pool,    [num_pages, page_size, H_kv, D] dtype
+ *   v_pool
+ *   page_table [B, max_pages_per_seq] int32 pool page ids on the device;
+ *              entries at or past ceil(kv_lens[b]/page_size) are never read,
+ *              every entry read must be in [0, num_pages) (else the kernel
+ *              reads zeros for that page and records device error code 2).
+ *   kv_lens    [B] int32 on the device, 0 <= kv_lens[b] <= max_pages_per_seq *
+ *              page_size (else clamped and device error code 2 recorded).  A
+ *              query row with no visible key gets o = 0 and lse = -inf.
+ *   o          [B,S_q,H_q,D] dtype output.
+ *   lse        [B,H_q,S_q] fp32 natural-log row sums, or NULL.
+ *   page_size  8, 16, 32, 64 or a multiple of 128 (else ATTN_ERR_UNSUPPORTED).
+ *   H_q % H_kv == 0; D 64 or 128; causal 0 or 1; scale finite and > 0.
+ *   B*S_q == 0 is a no-op.  Keys past kv_lens[b] in a page may hold any bit
+ *   pattern, NaN included: they never reach the output.
+ * Accumulation is fp32; P is rounded to the input dtype before P V.
+ * Allocates nothing.
+ */
+ATTN_API attn_status attn_extend_fwd(const void* q, const void* k_pool, const void* v_pool,
+                            const int32_t* page_table, const int32_t* kv_lens, void* o,
+                            float* lse, int B, int S_q, int H_q, int H_kv, int D, int page_size,
+                            int max_pages_per_seq, int num_pages, attn_dtype dtype, int causal,
+                            float scale, cudaStream_t stream);
+
+/*
  * Decode attention forward (one query per head, split KV, paged or contiguous
  * KV cache).
  *
@@ -154,7 +191,9 @@ ATTN_API const char* attn_last_error(void);
 /*
  * Read (and clear, if `clear` != 0) the device error word of the current
  * device: 0 when no kernel recorded an error, else (code << 16) | site, where
- * code 1 = a wait ran past its time limit.  Synchronizes the device first.
+ * code 1 = a wait ran past its time limit and code 2 = a kernel met an
+ * argument it cannot use (a kv_len outside the page table's capacity, a page
+ * id outside the pool).  Synchronizes the device first.
  * Returns ATTN_OK, or ATTN_ERR_DEVICE_TIMEOUT when the word was non-zero.
  */
 ATTN_API attn_status attn_device_error(int* word, int clear);

@@ -111,6 +111,43 @@ def test_decode_empty_batch_is_a_no_op():
     assert _decode(B=0, num_pages=0) == attn.ATTN_OK
 
 
+def _extend(**kw):
+    a = dict(q=16, k_pool=16, v_pool=16, page_table=16, kv_lens=16, o=16, lse=None, B=2, S_q=64,
+             H_q=8, H_kv=2, D=128, page_size=16, max_pages_per_seq=8, num_pages=16, dtype=1,
+             causal=1, scale=0.1, stream=None)
+    a.update(kw)
+    return attn.attn_extend_fwd(**a)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(H_kv=3), attn.ATTN_ERR_INVALID_ARG),
+    (dict(H_kv=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(S_q=-1), attn.ATTN_ERR_INVALID_ARG),
+    (dict(D=96), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(dtype=5), attn.ATTN_ERR_INVALID_ARG),
+    (dict(causal=3), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), attn.ATTN_ERR_INVALID_ARG),
+    (dict(page_size=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(page_size=4), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(page_size=48), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(page_size=192), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(max_pages_per_seq=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(num_pages=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(page_table=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(kv_lens=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(q=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(v_pool=8), attn.ATTN_ERR_INVALID_ARG),  # misaligned
+])
+def test_extend_rejects_bad_arguments(kw, code):
+    assert _extend(**kw) == code
+    assert attn.attn_last_error()
+
+
+def test_extend_empty_problem_is_a_no_op():
+    assert _extend(B=0, q=None, o=None) == attn.ATTN_OK
+    assert _extend(S_q=0) == attn.ATTN_OK
+
+
 def test_product_never_imports_the_oracle():
     pkg = os.path.join(ROOT, "attention_flash_attn_fwd_gb300")
     for dirpath, _, files in os.walk(pkg):
