@@ -117,6 +117,20 @@ bool decode_map(CUtensorMap* m, const void* base, int num_pages, int page_size, 
                                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
+// Extend tensor map over a pool [num_pages, page_size, H_kv, D] seen as 2-D:
+// dims (H_kv * D, num_pages * page_size), box (64, rows).
+bool extend_map(CUtensorMap* m, const void* base, int num_pages, int page_size, int H_kv, int D,
+                int box_rows, bool bf16) {
+  const uint64_t el = 2;
+  uint64_t dims[2] = {static_cast<uint64_t>(D) * H_kv,
+                      static_cast<uint64_t>(num_pages) * page_size};
+  uint64_t strides[1] = {el * D * H_kv};
+  uint32_t box[2] = {64, static_cast<uint32_t>(box_rows)};
+  return attn_host::encode_tiled_16bit(m, base, 2, dims, strides, box, bf16,
+                                       CU_TENSOR_MAP_SWIZZLE_128B,
+                                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+}
+
 int env_int(const char* name, int dflt) {
   const char* v = std::getenv(name);
   if (!v || !*v) return dflt;
@@ -247,6 +261,8 @@ attn_status attn_extend_fwd(const void* q, const void* k_pool, const void* v_poo
     return fail(ATTN_ERR_INVALID_ARG, "q, k_pool, v_pool and o must be 16-byte aligned");
   if (static_cast<int64_t>(max_pages_per_seq) * page_size > 0x7FFFFFFF)
     return fail(ATTN_ERR_UNSUPPORTED, "KV capacity exceeds 2^31 keys");
+  if ((static_cast<int64_t>(num_pages) + 1) * page_size > 0x7FFFFFFF)
+    return fail(ATTN_ERR_UNSUPPORTED, "KV pool exceeds 2^31 rows");
   if (static_cast<int64_t>(num_pages) * page_size * H_kv * D * 2 >= (int64_t(1) << 40) ||
       static_cast<int64_t>(B) * S_q * H_q * D * 2 >= (int64_t(1) << 40))
     return fail(ATTN_ERR_UNSUPPORTED, "tensor too large for one TMA descriptor");
@@ -264,8 +280,8 @@ attn_status attn_extend_fwd(const void* q, const void* k_pool, const void* v_poo
   CUtensorMap mq, mk, mv, mo;
   if (!prefill_map(&mq, q, B, H_q, S_q, D, true, bf16) ||
       !prefill_map(&mo, o, B, H_q, S_q, D, true, bf16) ||
-      !decode_map(&mk, k_pool, num_pages, page_size, H_kv, D, box_rows, bf16) ||
-      !decode_map(&mv, v_pool, num_pages, page_size, H_kv, D, box_rows, bf16))
+      !extend_map(&mk, k_pool, num_pages, page_size, H_kv, D, box_rows, bf16) ||
+      !extend_map(&mv, v_pool, num_pages, page_size, H_kv, D, box_rows, bf16))
     return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed for an extend tensor");
 
   attn_sm103a::PrefillParams p{};

@@ -34,8 +34,8 @@ cudaError_t prefill_launch(const CUtensorMap& q, const CUtensorMap& k, const CUt
                            cudaStream_t stream);
 
 // Extend form: q/o maps as BSHD (D, H, S_q, B); k/v maps over the pool
-// [num_pages, page_size, H_kv, D] as (D, H_kv, page_size, num_pages) with box
-// (64, 1, min(page_size, 128), 1).
+// [num_pages, page_size, H_kv, D] as 2-D (H_kv * D, num_pages * page_size)
+// with box (64, min(page_size, 128)).
 cudaError_t extend_launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                           const CUtensorMap& o, const PrefillParams& p, int D, bool bf16,
                           cudaStream_t stream);
