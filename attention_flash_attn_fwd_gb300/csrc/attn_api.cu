@@ -305,6 +305,9 @@ attn_status attn_extend_fwd(const void* q, const void* k_pool, const void* v_poo
   p.H_kv = H_kv;
   p.k_pool = k_pool;
   p.v_pool = v_pool;
+  // Pages of at most 16 keys make the page-box gather the bottleneck: CTA
+  // pairs that share a kv head split it (the group must be even).
+  p.pair = (p.group % 2 == 0 && page_size <= 16) ? 1 : 0;
   cudaError_t e = attn_sm103a::extend_launch(mq, mk, mv, mo, p, D, bf16, stream);
   if (e != cudaSuccess) return fail_cuda(e, "extend launch");
   return ATTN_OK;

@@ -25,6 +25,7 @@ struct PrefillParams {
   int H_kv;
   const void* k_pool;         // [num_pages, page_size, H_kv, D]
   const void* v_pool;
+  int pair;                   // 1: CTA pairs (clusters of 2) share K/V tiles; needs an even group
 };
 
 // Tensor maps: 16-bit elements, 128-byte swizzle, box = 64 columns x

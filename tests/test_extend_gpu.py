@@ -132,3 +132,29 @@ def test_extend_full_size_sampled_heads():
             ref_o, ref_lse = _ref(sub, case.causal, case.scale)
             assert_close(o[b:b + 1, :, h:h + 1], ref_o, "C6 b=%d h=%d" % (b, h))
             assert_lse_close(lse[b:b + 1, h:h + 1], ref_lse, "C6 lse b=%d h=%d" % (b, h))
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_extend_paired_ctas_match_unpaired(D):
+    """With 16-token pages and an even GQA group, CTA pairs share the page
+    gather; the same keys laid out in 128-token pages take the unpaired path.
+    Both must give the same bits."""
+    case = workloads.ExtendCase("t", 3, 333, 8, 2, D, 0, 1500, page_size=16, seed=29)
+    inp = workloads.make_extend(case, prefix_lens=[1500, 5, 700])
+    o16, l16 = _gpu(inp, True, case.scale)
+    B, H_kv = 3, 2
+    cap = inp.max_pages * 16
+    n128 = -(-cap // 128)
+    k128 = torch.zeros(B * n128, 128, H_kv, D, dtype=inp.k.dtype)
+    v128 = torch.zeros_like(k128)
+    for b in range(B):
+        n = int(inp.kv_lens[b])
+        t = torch.arange(n)
+        phys = inp.page_table[b].long()[t // 16]
+        rows = b * n128 * 128 + t
+        k128.view(-1, H_kv, D)[rows] = inp.k[phys, t % 16]
+        v128.view(-1, H_kv, D)[rows] = inp.v[phys, t % 16]
+    pt128 = torch.arange(B * n128, dtype=torch.int32).view(B, n128)
+    re = workloads.ExtendInputs(inp.q, k128, v128, inp.kv_lens, pt128, 128, n128)
+    o128, l128 = _gpu(re, True, case.scale)
+    assert torch.equal(o16, o128) and torch.equal(l16, l128)
