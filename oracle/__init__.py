@@ -20,7 +20,10 @@ are stated at the top of ``attn_oracle.c``:
   the fake-page-table test fixture);
 * extend: S_q new queries per sequence against its ``kv_len`` keys in the
   paged pool, bottom-right causal per sequence (Wave February 2025 Release,
-  "Extend Attention"; WAVE MLSys 2026 summary, Integration: SGLang extend).
+  "Extend Attention"; WAVE MLSys 2026 summary, Integration: SGLang extend);
+* FP8 prefill: the prefill definition on E4M3 codes times per-tensor descale
+  factors (Wave February 2025 Release, "FAv3 - FP8"), E4M3 decoded from the
+  OCP 8-bit floating point definition.
 
 Every function here is pinned by ``tests/test_oracle.py`` against library
 routines, closed forms and analytic fixtures; no part is left unpinned.
@@ -82,6 +85,8 @@ def _load():
             lib.oracle_extend_f64.argtypes = [dp, dp, dp, ip, ip, dp, dp, L, L, L, L, L, L,
                                               L, ctypes.c_int, ctypes.c_double, ctypes.c_int]
             lib.oracle_extend_f64.restype = ctypes.c_int
+            lib.oracle_e4m3_decode.argtypes = [ctypes.POINTER(ctypes.c_uint8), dp, L]
+            lib.oracle_e4m3_decode.restype = None
             _lib = lib
     return _lib
 
@@ -209,3 +214,27 @@ def extend(q, k_pool, v_pool, page_table, kv_lens, *, causal: bool, scale: float
     if rc != 0:
         raise RuntimeError("oracle_extend_f64 failed (rc=%d)" % rc)
     return o, lse
+
+
+def decode_e4m3(codes) -> np.ndarray:
+    """Float64 values of E4M3 codes (a uint8 numpy array or a torch uint8 /
+    float8_e4m3fn tensor), same shape."""
+    if hasattr(codes, "detach"):
+        t = codes.detach().to("cpu")
+        if t.dtype != __import__("torch").uint8:
+            t = t.view(__import__("torch").uint8)
+        codes = t.numpy()
+    u8 = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8))
+    out = np.empty(u8.shape, dtype=np.float64)
+    _load().oracle_e4m3_decode(u8.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)), _dptr(out),
+                               u8.size)
+    return out
+
+
+def prefill_fp8(q, k, v, *, descale_q: float, descale_k: float, descale_v: float, causal: bool,
+                scale: float, layout: int = BHSD, n_threads: int | None = None):
+    """FP8 prefill in float64: Q, K, V are E4M3 codes (layouts as ``prefill``),
+    real values descale_x * value(code).  Returns ``(o, lse)`` like ``prefill``."""
+    return prefill(decode_e4m3(q) * float(descale_q), decode_e4m3(k) * float(descale_k),
+                   decode_e4m3(v) * float(descale_v), causal=causal, scale=scale, layout=layout,
+                   n_threads=n_threads)

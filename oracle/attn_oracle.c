@@ -46,6 +46,14 @@
  * its kv_lens[b] cached keys (which include the new tokens), causal
  * alignment bottom-right per sequence, kv head h / (H_q / H_kv).
  *
+ * FP8 prefill ("FAv3 - FP8", Wave February 2025 Release, FlashDecoding list)
+ * is the same definition on inputs stored as 8-bit E4M3 codes with one
+ * descale factor per tensor: x = descale * value(code).  value() follows the
+ * OCP 8-bit floating point E4M3 format: sign bit, 4 exponent bits with bias
+ * 7, 3 mantissa bits; exponent 0 encodes subnormals m/8 * 2^-6; the all-ones
+ * exponent with all-ones mantissa is NaN; there is no infinity (so the
+ * largest finite value is 1.75 * 2^8 = 448).
+ *
  * Rows are independent; they are spread over POSIX threads.
  */
 #include <math.h>
@@ -354,4 +362,24 @@ int oracle_extend_f64(const double *q, const double *k_pool, const double *v_poo
     extend_job J = {q, k_pool, v_pool, page_table, kv_lens, o, lse, B, S_q, H_q, H_kv, D,
                     page_size, max_pages, causal, scale, 0};
     return run_threads(extend_worker, &J, n_threads);
+}
+
+/* ------------------------------------------------------------------- e4m3 */
+
+/* Decode n E4M3 codes to float64 (exact: every E4M3 value is a double). */
+void oracle_e4m3_decode(const uint8_t *in, double *out, long n) {
+    for (long i = 0; i < n; ++i) {
+        const unsigned c = in[i];
+        const int sign = (c >> 7) & 1;
+        const int e = (c >> 3) & 0xF;
+        const int m = c & 0x7;
+        double v;
+        if (e == 0xF && m == 0x7)
+            v = NAN;
+        else if (e == 0)
+            v = ldexp((double)m / 8.0, -6);
+        else
+            v = ldexp(1.0 + (double)m / 8.0, e - 7);
+        out[i] = sign ? -v : v;
+    }
 }

@@ -383,6 +383,50 @@ def test_extend_without_prefix_equals_causal_prefill():
         np.testing.assert_allclose(lse[b], plse[0], rtol=0, atol=TOL)
 
 
+# -------------------------------------------------------------------- fp8
+
+
+def test_e4m3_decode_matches_torch_for_every_code():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ours = oracle.decode_e4m3(codes.numpy())
+    ref = codes.view(torch.float8_e4m3fn).double().numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan) and int(nan.sum()) == 2  # 0x7f and 0xff
+    np.testing.assert_array_equal(ours[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(ours[~nan]), np.signbit(ref[~nan]))
+
+
+def test_e4m3_decode_closed_forms():
+    """Values fixed by the format definition: 1 = 0x38, largest 448 = 0x7e,
+    smallest subnormal 2^-9 = 0x01, smallest normal 2^-6 = 0x08, -2 = 0xc0."""
+    v = oracle.decode_e4m3(np.array([0x38, 0x7E, 0x01, 0x08, 0xC0, 0x00, 0x07, 0x3C],
+                                    dtype=np.uint8))
+    assert list(v) == [1.0, 448.0, 2.0 ** -9, 2.0 ** -6, -2.0, 0.0, 7 * 2.0 ** -9, 1.5]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_prefill_fp8_matches_torch_sdpa(causal):
+    case = workloads.Fp8PrefillCase("t", 2, 3, 40, 75, 32, "bhsd", causal, seed=31)
+    q8, k8, v8, dq, dk, dv = workloads.make_prefill_fp8(case)
+    o, lse = oracle.prefill_fp8(q8, k8, v8, descale_q=dq, descale_k=dk, descale_v=dv,
+                                causal=causal, scale=case.scale)
+    Q, K, V = q8.double() * dq, k8.double() * dk, v8.double() * dv
+    mask = _bottom_right(40, 75) if causal else None
+    torch.testing.assert_close(torch.from_numpy(o), _sdpa_ref(Q, K, V, case.scale, mask),
+                               rtol=0, atol=TOL)
+    torch.testing.assert_close(torch.from_numpy(lse), _lse_ref(Q, K, case.scale, mask), rtol=0,
+                               atol=TOL)
+
+
+def test_fp8_quantization_is_within_half_a_step():
+    """The input recipe: codes * descale reproduce x within half an E4M3 step."""
+    x = torch.randn(1000, generator=torch.Generator().manual_seed(3))
+    q8, d = workloads.quantize_e4m3(x)
+    y = torch.from_numpy(oracle.decode_e4m3(q8)) * d
+    rel = ((y - x.double()).abs() / x.double().abs().clamp_min(2.0 ** -6 * d)).max().item()
+    assert rel <= 2.0 ** -4 + 1e-12
+
+
 # --------------------------------------------------------- planted mistakes
 
 _MUTANTS = {
@@ -405,6 +449,9 @@ _MUTANTS = {
     "extend_lse_index": ("J->lse + (size_t)((b * J->H_q + h) * J->S_q + i)",
                          "J->lse + (size_t)((b * J->S_q + i) * J->H_q + h)"),
     "v_from_k": ("o_row[d] += w * v_seq[t * D + d];", "o_row[d] += w * k_seq[t * D + d];"),
+    "e4m3_bias_8": ("ldexp(1.0 + (double)m / 8.0, e - 7)", "ldexp(1.0 + (double)m / 8.0, e - 8)"),
+    "e4m3_subnormal_as_normal": ("v = ldexp((double)m / 8.0, -6);",
+                                 "v = ldexp(1.0 + (double)m / 8.0, -7);"),
 }
 
 
@@ -415,6 +462,7 @@ def _pins_pass() -> bool:
         lambda: test_prefill_matches_torch_sdpa(2, 1, 64, 64, 128, False, "bhsd"),
         lambda: test_decode_matches_torch_sdpa(True, 8, 2),
         lambda: test_extend_matches_torch_sdpa(True, 8, 2, 8),
+        lambda: test_e4m3_decode_matches_torch_for_every_code(),
     ] + [lambda p=p: test_golden_fixture(p)
          for p in sorted(glob.glob(os.path.join(GOLDEN, "*.json")))]
     for c in checks:
@@ -448,6 +496,8 @@ def test_mutants_are_caught(name):
         mutant.oracle_decode_f64.restype = ctypes.c_int
         mutant.oracle_extend_f64.argtypes = saved.oracle_extend_f64.argtypes
         mutant.oracle_extend_f64.restype = ctypes.c_int
+        mutant.oracle_e4m3_decode.argtypes = saved.oracle_e4m3_decode.argtypes
+        mutant.oracle_e4m3_decode.restype = None
         oracle._lib = mutant
         try:
             assert not _pins_pass(), "pins did not catch planted mistake %r" % name

@@ -19,6 +19,11 @@ Recipe (every draw uses a CPU ``torch.Generator`` seeded with ``seed``):
   data pages placed by the permutation, one extra poison page (all 1e4) is
   appended, unused page-table entries point at it, and page tail slots hold
   1e4 too, so a masking bug is loud but never reads outside the pool.
+* FP8 prefill: Q, K, V drawn as for prefill in float32 (times ``std``), then
+  each tensor is quantized on its own: descale = max|x| / 448 and the E4M3
+  codes are ``(x / descale)`` rounded by PyTorch's float8_e4m3fn conversion
+  (round to nearest even).  The codes and the three descale factors are the
+  inputs; nothing of the attention arithmetic happens here.
 * extend (prefill of new tokens against a paged cache): first the cached
   prefix lengths (``randint`` uniform on [prefix_min, prefix_max]) unless
   given, ``kv_len_b = prefix_b + S_q``; then Q [B,S_q,H_q,D]; then per
@@ -146,6 +151,35 @@ C5 = DecodeCase("decode_paged16_bf16_b32_hq32_hkv8_d128", 32, 32, 8, 128, 1, 327
                 paged=True)
 
 
+@dataclass(frozen=True)
+class Fp8PrefillCase:
+    """Prefill on E4M3 inputs with per-tensor descale factors; O in ``out_dtype``."""
+    name: str
+    B: int
+    H: int
+    S_q: int
+    S_kv: int
+    D: int
+    layout: str
+    causal: bool
+    out_dtype: str = "bf16"
+    std: float = 1.0
+    seed: int = 0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+    def flops(self) -> float:
+        return 4.0 * self.B * self.H * self.D * visible_pairs(self.S_q, self.S_kv, self.causal)
+
+
+# The BHSD prefill shape of C2 with E4M3 inputs (the pages' "FAv3 - FP8" item).
+C7 = Fp8PrefillCase("prefill_fp8e4m3_bhsd_b4_h32_s4096_d128", 4, 32, 4096, 4096, 128, "bhsd",
+                    False)
+C7_CAUSAL = Fp8PrefillCase("prefill_fp8e4m3_bhsd_b4_h32_s4096_d128_causal", 4, 32, 4096, 4096,
+                           128, "bhsd", True)
+
 # Prefix-cached prefill: 8 requests of 1024 new tokens each on top of cached
 # prefixes of up to 15360 tokens, Llama-3-8B-like GQA heads, 16-token pages.
 C6 = ExtendCase("extend_paged16_bf16_b8_sq1024_hq32_hkv8_d128_causal", 8, 1024, 32, 8, 128, 0,
@@ -177,6 +211,25 @@ def make_prefill(case: PrefillCase):
     k = _randn(g, prefill_shape(case.B, case.H, case.S_kv, case.D, case.layout), case.std, dt)
     v = _randn(g, prefill_shape(case.B, case.H, case.S_kv, case.D, case.layout), case.std, dt)
     return q, k, v
+
+
+def quantize_e4m3(x: torch.Tensor):
+    """Per-tensor E4M3 quantization: returns (codes as float8_e4m3fn, descale)."""
+    amax = float(x.abs().max())
+    descale = amax / 448.0 if amax > 0 else 1.0
+    return (x / descale).to(torch.float8_e4m3fn), descale
+
+
+def make_prefill_fp8(case: Fp8PrefillCase):
+    """Return (q8, k8, v8, dq, dk, dv): float8_e4m3fn CPU tensors and descales."""
+    g = _gen(case.seed)
+    qs = prefill_shape(case.B, case.H, case.S_q, case.D, case.layout)
+    ks = prefill_shape(case.B, case.H, case.S_kv, case.D, case.layout)
+    q = _randn(g, qs, case.std, torch.float32)
+    k = _randn(g, ks, case.std, torch.float32)
+    v = _randn(g, ks, case.std, torch.float32)
+    (q8, dq), (k8, dk), (v8, dv) = quantize_e4m3(q), quantize_e4m3(k), quantize_e4m3(v)
+    return q8, k8, v8, dq, dk, dv
 
 
 @dataclass
