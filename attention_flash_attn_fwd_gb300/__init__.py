@@ -43,7 +43,7 @@ _STATUS_NAMES = {
 }
 
 # Names the header exports (checked against include/attn_gb300.h by the tests).
-EXPORTED = ("attn_prefill_fwd", "attn_extend_fwd", "attn_decode_fwd", "attn_decode_fwd_noalloc",
+EXPORTED = ("attn_prefill_fwd", "attn_prefill_fp8_fwd", "attn_extend_fwd", "attn_decode_fwd", "attn_decode_fwd_noalloc",
             "attn_last_error",
             "attn_device_error", "attn_set_wait_limit_ns", "attn_release_workspace",
             "attn_version")
@@ -77,6 +77,9 @@ def lib() -> ctypes.CDLL:
             L.attn_prefill_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, cf,
                                            vp]
             L.attn_prefill_fwd.restype = ci
+            L.attn_prefill_fp8_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci,
+                                               cf, cf, cf, cf, vp]
+            L.attn_prefill_fp8_fwd.restype = ci
             L.attn_extend_fwd.argtypes = [vp, vp, vp, i32p, i32p, vp, vp, ci, ci, ci, ci, ci, ci,
                                           ci, ci, ci, ci, cf, vp]
             L.attn_extend_fwd.restype = ci
@@ -117,6 +120,13 @@ def attn_prefill_fwd(q, k, v, o, lse, B, H, S_q, S_kv, D, layout, dtype, causal,
     """C ``attn_prefill_fwd``; pointers and stream as ints.  Returns the status."""
     return lib().attn_prefill_fwd(q, k, v, o, lse, B, H, S_q, S_kv, D, layout, dtype, causal,
                                   scale, stream)
+
+
+def attn_prefill_fp8_fwd(q, k, v, o, lse, B, H, S_q, S_kv, D, layout, out_dtype, causal, scale,
+                         descale_q, descale_k, descale_v, stream) -> int:
+    """C ``attn_prefill_fp8_fwd``; pointers and stream as ints.  Returns the status."""
+    return lib().attn_prefill_fp8_fwd(q, k, v, o, lse, B, H, S_q, S_kv, D, layout, out_dtype,
+                                      causal, scale, descale_q, descale_k, descale_v, stream)
 
 
 def attn_extend_fwd(q, k_pool, v_pool, page_table, kv_lens, o, lse, B, S_q, H_q, H_kv, D,
@@ -235,6 +245,48 @@ def prefill(q, k, v, *, causal: bool = False, scale: float | None = None,
     return (out, lse) if return_lse else out
 
 
+def prefill_fp8(q, k, v, *, descale_q: float, descale_k: float, descale_v: float,
+                causal: bool = False, scale: float | None = None, layout: str = "bhsd",
+                out_dtype=None, out=None, lse=None, return_lse: bool = False, stream=None):
+    """FP8 (E4M3) attention forward over torch CUDA tensors.
+
+    ``q``, ``k``, ``v``: torch.float8_e4m3fn (or uint8 holding E4M3 codes) in
+    the layout's shape; real values are ``descale_x * value``.  ``o`` is
+    bfloat16 unless ``out_dtype`` (torch.float16 / torch.bfloat16) says
+    otherwise.  D must be 128.
+    """
+    torch = _torch()
+    _require_cuda(q, k, v, out, lse)
+    for t in (q, k, v):
+        if t.dtype not in (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8)):
+            raise TypeError("FP8 prefill inputs must be float8_e4m3fn or uint8 codes")
+    if layout == "bhsd":
+        B, H, S_q, D = q.shape
+        S_kv = k.shape[2]
+        code = ATTN_BHSD
+    elif layout == "bshd":
+        B, S_q, H, D = q.shape
+        S_kv = k.shape[1]
+        code = ATTN_BSHD
+    else:
+        raise ValueError("layout must be 'bhsd' or 'bshd'")
+    if k.shape != v.shape:
+        raise ValueError("k and v must have the same shape")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty(q.shape, device=q.device,
+                          dtype=out_dtype if out_dtype is not None else torch.bfloat16)
+    if return_lse and lse is None:
+        lse = torch.empty((B, H, S_q), device=q.device, dtype=torch.float32)
+    _check(attn_prefill_fp8_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                lse.data_ptr() if lse is not None else None, B, H, S_q, S_kv, D,
+                                code, _dtype_code(out), int(bool(causal)), float(scale),
+                                float(descale_q), float(descale_k), float(descale_v),
+                                _stream_handle(stream)))
+    return (out, lse) if return_lse else out
+
+
 def extend(q, k_pool, v_pool, page_table, kv_lens, *, causal: bool = True,
            scale: float | None = None, num_pages: int | None = None, out=None, lse=None,
            return_lse: bool = False, stream=None):
@@ -313,4 +365,4 @@ def check_device_error() -> None:
 
 
 __all__ = [n for n in dir() if n.startswith(("attn_", "ATTN_"))] + [
-    "AttnError", "prefill", "extend", "decode", "lib", "library_path", "check_device_error", "EXPORTED"]
+    "AttnError", "prefill", "prefill_fp8", "extend", "decode", "lib", "library_path", "check_device_error", "EXPORTED"]

@@ -10,6 +10,7 @@
 #include <cstdlib>
 #include <mutex>
 #include <string>
+#include <unordered_map>
 
 #include "../../include/attn_gb300.h"
 #include "decode_sm103a.h"
@@ -49,8 +50,13 @@ struct DeviceState {
   std::mutex mu;
   int* err_word = nullptr;    // device address of g_device_error_word
   int num_sms = 0;
-  void* workspace = nullptr;  // decode split partials
-  size_t workspace_bytes = 0;
+  // Decode split partials, one buffer per stream: calls on different streams
+  // may overlap on the GPU, calls on one stream run in order.
+  struct Workspace {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+  };
+  std::unordered_map<cudaStream_t, Workspace> workspaces;
 };
 
 DeviceState g_dev[kMaxDevices];
@@ -101,6 +107,26 @@ bool prefill_map(CUtensorMap* m, const void* base, int B, int H, int S, int D, b
   }
   return attn_host::encode_tiled_16bit(m, base, 4, dims, strides, box, bf16,
                                        CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// FP8 prefill tensor map over E4M3 bytes, layouts as prefill_map; box 128
+// columns (128 bytes) x 128 rows.
+bool prefill_map_fp8(CUtensorMap* m, const void* base, int B, int H, int S, int D, bool bshd) {
+  uint64_t dims[4], strides[3];
+  uint32_t box[4];
+  if (!bshd) {
+    dims[0] = D; dims[1] = S; dims[2] = H; dims[3] = B;
+    strides[0] = D; strides[1] = static_cast<uint64_t>(D) * S;
+    strides[2] = static_cast<uint64_t>(D) * S * H;
+    box[0] = 128; box[1] = attn_sm103a::prefill_box_rows(); box[2] = 1; box[3] = 1;
+  } else {
+    dims[0] = D; dims[1] = H; dims[2] = S; dims[3] = B;
+    strides[0] = D; strides[1] = static_cast<uint64_t>(D) * H;
+    strides[2] = static_cast<uint64_t>(D) * H * S;
+    box[0] = 128; box[1] = 1; box[2] = attn_sm103a::prefill_box_rows(); box[3] = 1;
+  }
+  return attn_host::encode_tiled_8bit(m, base, 4, dims, strides, box,
+                                      CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // Decode tensor map over a pool [num_pages, page_size, H_kv, D]: dims
@@ -218,6 +244,7 @@ attn_status attn_prefill_fwd(const void* q, const void* k, const void* v, void* 
 
   attn_sm103a::PrefillParams p{};
   p.lse = lse;
+  p.o_scale = 1.f;
   p.B = B;
   p.H = H;
   p.S_q = S_q;
@@ -230,6 +257,73 @@ attn_status attn_prefill_fwd(const void* q, const void* k, const void* v, void* 
   p.wait_limit_ns = g_wait_limit_ns.load();
   cudaError_t e = attn_sm103a::prefill_launch(mq, mk, mv, mo, p, D, bf16, stream);
   if (e != cudaSuccess) return fail_cuda(e, "prefill launch");
+  return ATTN_OK;
+}
+
+attn_status attn_prefill_fp8_fwd(const void* q, const void* k, const void* v, void* o,
+                                 float* lse, int B, int H, int S_q, int S_kv, int D,
+                                 attn_layout layout, attn_dtype out_dtype, int causal, float scale,
+                                 float descale_q, float descale_k, float descale_v,
+                                 cudaStream_t stream) {
+  if (B < 0 || H < 0 || S_q < 0 || S_kv < 0)
+    return fail(ATTN_ERR_INVALID_ARG, "B, H, S_q and S_kv must be >= 0");
+  if (layout != ATTN_BHSD && layout != ATTN_BSHD)
+    return fail(ATTN_ERR_INVALID_ARG, "layout must be ATTN_BHSD or ATTN_BSHD");
+  if (out_dtype != ATTN_F16 && out_dtype != ATTN_BF16)
+    return fail(ATTN_ERR_INVALID_ARG, "out_dtype must be ATTN_F16 or ATTN_BF16");
+  if (causal != 0 && causal != 1) return fail(ATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (!(std::isfinite(scale) && scale > 0.f))
+    return fail(ATTN_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (!(std::isfinite(descale_q) && descale_q > 0.f && std::isfinite(descale_k) &&
+        descale_k > 0.f && std::isfinite(descale_v) && descale_v > 0.f))
+    return fail(ATTN_ERR_INVALID_ARG, "descale factors must be finite and > 0");
+  if (D != 128) return fail(ATTN_ERR_UNSUPPORTED, "the FP8 form supports D = 128 only");
+  if (static_cast<int64_t>(B) * H * S_q == 0) return ATTN_OK;  // nothing to compute
+  if (!q || !o || (S_kv > 0 && (!k || !v)))
+    return fail(ATTN_ERR_INVALID_ARG, "q, k, v and o must be non-NULL");
+  if (!aligned16(q) || !aligned16(o) || (S_kv > 0 && (!aligned16(k) || !aligned16(v))))
+    return fail(ATTN_ERR_INVALID_ARG, "q, k, v and o must be 16-byte aligned");
+  const int64_t elems = static_cast<int64_t>(B) * H * (S_q > S_kv ? S_q : S_kv) * D;
+  if (elems * 2 >= (int64_t(1) << 40))
+    return fail(ATTN_ERR_UNSUPPORTED, "tensor too large for one TMA descriptor");
+  const int rows = attn_sm103a::prefill_rows_per_cta();
+  const int64_t n_qb = (S_q + rows - 1) / rows;
+  if (static_cast<int64_t>(B) * H * n_qb > 0x7FFFFFFF)
+    return fail(ATTN_ERR_UNSUPPORTED, "grid too large");
+
+  DeviceState* st = nullptr;
+  attn_status s = device_state(&st);
+  if (s != ATTN_OK) return s;
+
+  const bool bshd = layout == ATTN_BSHD;
+  CUtensorMap mq, mk, mv, mo;
+  const int S_kv_map = S_kv > 0 ? S_kv : 1;
+  const void* kb = S_kv > 0 ? k : q;
+  const void* vb = S_kv > 0 ? v : q;
+  if (!prefill_map_fp8(&mq, q, B, H, S_q, D, bshd) ||
+      !prefill_map_fp8(&mk, kb, B, H, S_kv_map, D, bshd) ||
+      !prefill_map_fp8(&mv, vb, B, H, S_kv_map, D, bshd) ||
+      !prefill_map(&mo, o, B, H, S_q, D, bshd, out_dtype == ATTN_BF16))
+    return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed for an FP8 prefill tensor");
+
+  attn_sm103a::PrefillParams p{};
+  p.lse = lse;
+  p.o_scale = descale_v;
+  p.B = B;
+  p.H = H;
+  p.S_q = S_q;
+  p.S_kv = S_kv;
+  p.num_q_blocks = static_cast<int>(n_qb);
+  p.causal = causal;
+  p.bshd = bshd ? 1 : 0;
+  // scores of the stored codes times descale_q * descale_k are the real ones
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * descale_q * descale_k *
+                                    1.4426950408889634);
+  p.err = st->err_word;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  cudaError_t e =
+      attn_sm103a::prefill_fp8_launch(mq, mk, mv, mo, p, out_dtype == ATTN_BF16, stream);
+  if (e != cudaSuccess) return fail_cuda(e, "FP8 prefill launch");
   return ATTN_OK;
 }
 
@@ -286,6 +380,7 @@ attn_status attn_extend_fwd(const void* q, const void* k_pool, const void* v_poo
 
   attn_sm103a::PrefillParams p{};
   p.lse = lse;
+  p.o_scale = 1.f;
   p.B = B;
   p.H = H_q;
   p.S_q = S_q;
@@ -382,9 +477,11 @@ attn_status attn_decode_fwd(const void* q, const void* k_pool, const void* v_poo
   // Workspace: o_part [B, H_q, max_splits, D] + lse_part [B, H_q, max_splits].
   const size_t rows_ws = static_cast<size_t>(B) * H_q * max_splits;
   const size_t need = rows_ws * D * sizeof(float) + rows_ws * sizeof(float);
+  void* workspace = nullptr;
   {
     std::lock_guard<std::mutex> lk(st->mu);
-    if (st->workspace_bytes < need) {
+    DeviceState::Workspace& w = st->workspaces[stream];
+    if (w.bytes < need) {
       cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
       cudaError_t e = cudaStreamIsCapturing(stream, &cs);
       if (e != cudaSuccess) return fail_cuda(e, "cudaStreamIsCapturing");
@@ -392,11 +489,11 @@ attn_status attn_decode_fwd(const void* q, const void* k_pool, const void* v_poo
         return fail(ATTN_ERR_NO_MEMORY,
                     "decode workspace must grow but the stream is capturing; call once before "
                     "capture with the largest shapes");
-      if (st->workspace) {
-        cudaDeviceSynchronize();
-        cudaFree(st->workspace);
-        st->workspace = nullptr;
-        st->workspace_bytes = 0;
+      if (w.ptr) {
+        cudaStreamSynchronize(stream);
+        cudaFree(w.ptr);
+        w.ptr = nullptr;
+        w.bytes = 0;
       }
       void* ws = nullptr;
       e = cudaMalloc(&ws, need);
@@ -404,9 +501,10 @@ attn_status attn_decode_fwd(const void* q, const void* k_pool, const void* v_poo
         cudaGetLastError();
         return fail(ATTN_ERR_NO_MEMORY, std::string("workspace cudaMalloc: ") + cudaGetErrorString(e));
       }
-      st->workspace = ws;
-      st->workspace_bytes = need;
+      w.ptr = ws;
+      w.bytes = need;
     }
+    workspace = w.ptr;
   }
 
   const bool bf16 = dtype == ATTN_BF16;
@@ -420,7 +518,7 @@ attn_status attn_decode_fwd(const void* q, const void* k_pool, const void* v_poo
   p.q = q;
   p.page_table = page_table;
   p.kv_lens = kv_lens;
-  p.o_part = static_cast<float*>(st->workspace);
+  p.o_part = static_cast<float*>(workspace);
   p.lse_part = p.o_part + rows_ws * D;
   p.B = B;
   p.H_q = H_q;
@@ -444,12 +542,11 @@ attn_status attn_release_workspace(void) {
   attn_status s = device_state(&st);
   if (s != ATTN_OK) return s;
   std::lock_guard<std::mutex> lk(st->mu);
-  if (st->workspace) {
+  if (!st->workspaces.empty()) {
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceSynchronize");
-    cudaFree(st->workspace);
-    st->workspace = nullptr;
-    st->workspace_bytes = 0;
+    for (auto& kv : st->workspaces) cudaFree(kv.second.ptr);
+    st->workspaces.clear();
   }
   return ATTN_OK;
 }

@@ -43,6 +43,13 @@
 // query heads 2k and 2k+1 of one kv head and one query block, each CTA
 // issues every other page box multicast to both, and each MMA warp releases
 // a K/V stage in both CTAs (0.96 -> 0.80 ms with 16-token pages).
+//
+// The FP8 form (kFp8; Wave February 2025 Release, "FAv3 - FP8") reads E4M3
+// Q, K, V: tiles are half the bytes (one 128-byte swizzled panel holds a
+// 128-wide row), both products run as `.kind::f8f6f4` MMAs (K = 32 per
+// instruction), P is written to tensor memory as E4M3 (four per column) and
+// the per-tensor descale factors fold into the softmax scale and the final
+// 1/l.  O (bf16 or fp16) is staged in its own shared-memory tiles.
 #include "prefill_sm103a.h"
 #include "sm103a_ptx.cuh"
 
@@ -66,11 +73,18 @@ static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsControl <= kThreads * kRegsAtL
               "register split exceeds the block's launch allocation");
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-template <int D>
+template <int D, bool kFp8 = false>
 struct Cfg {
-  static constexpr int kTileBytes = kBM * D * 2;          // one Q/K/V/O tile
-  static constexpr int kStages = (D == 128) ? 5 : 10;     // KV ring depth
-  static constexpr int kSmemData = kTiles * kTileBytes + kStages * kTileBytes;
+  static constexpr int kElt = kFp8 ? 1 : 2;               // bytes per Q/K/V element
+  static constexpr int kTileBytes = kBM * D * kElt;       // one Q/K/V tile
+  static constexpr int kOTileBytes = kBM * D * 2;         // one O tile (16-bit)
+  static constexpr int kBoxCols = 128 / kElt;             // columns per 128-byte TMA box
+  static constexpr int kBoxes = D / kBoxCols;             // boxes (swizzle panels) per row
+  static constexpr int kKeysPerPV = 32 / kElt;            // keys per PV MMA instruction
+  static constexpr int kStages = kFp8 ? 8 : ((D == 128) ? 5 : 10);  // KV ring depth
+  // FP8: O has its own staging tiles (a Q tile is too small to hold it).
+  static constexpr int kOStageOff = kTiles * kTileBytes + kStages * kTileBytes;
+  static constexpr int kSmemData = kOStageOff + (kFp8 ? kTiles * kOTileBytes : 0);
   static constexpr int kSmemBytes = kSmemData + 1024 /*align*/ + 256 /*barriers*/;
   // tensor-memory columns of S_t and O_t
   __device__ static constexpr uint32_t col_s(int t) { return t * 128u; }
@@ -253,13 +267,13 @@ __device__ __forceinline__ int extend_kv_len(int b, const PrefillParams& p) {
   return kv;
 }
 
-template <int D, bool kBF16, bool kPaged>
+template <int D, bool kBF16, bool kPaged, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_o, const PrefillParams p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, kFp8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -332,21 +346,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_map(&tm_v);
       for (int t = 0; t < kTiles; ++t) {
         mbar_arrive_expect_tx(&ctl->q_full[t], C::kTileBytes);
-        for (int x = 0; x < D / 64; ++x)
-          load_box(s_q + t * C::kTileBytes + x * (kBM * 128), &tm_q, &ctl->q_full[t], x * 64,
-                   row_base + t * kBM, h, b, p.bshd);
+        for (int x = 0; x < C::kBoxes; ++x)
+          load_box(s_q + t * C::kTileBytes + x * (kBM * 128), &tm_q, &ctl->q_full[t],
+                   x * C::kBoxCols, row_base + t * kBM, h, b, p.bshd);
       }
       for (int j = 0; j < min(n_all, kL2PrefetchTiles); ++j)
-        for (int x = 0; x < D / 64; ++x) {
-          prefetch_box(&tm_k, x * 64, j * kBN, h, b, p.bshd);
-          prefetch_box(&tm_v, x * 64, j * kBN, h, b, p.bshd);
+        for (int x = 0; x < C::kBoxes; ++x) {
+          prefetch_box(&tm_k, x * C::kBoxCols, j * kBN, h, b, p.bshd);
+          prefetch_box(&tm_v, x * C::kBoxCols, j * kBN, h, b, p.bshd);
         }
       volatile int* abort_flag = &ctl->abort;
       for (int j = 0; j < n_all && !*abort_flag; ++j) {
         if (j + kL2PrefetchTiles < n_all)
-          for (int x = 0; x < D / 64; ++x) {
-            prefetch_box(&tm_k, x * 64, (j + kL2PrefetchTiles) * kBN, h, b, p.bshd);
-            prefetch_box(&tm_v, x * 64, (j + kL2PrefetchTiles) * kBN, h, b, p.bshd);
+          for (int x = 0; x < C::kBoxes; ++x) {
+            prefetch_box(&tm_k, x * C::kBoxCols, (j + kL2PrefetchTiles) * kBN, h, b, p.bshd);
+            prefetch_box(&tm_v, x * C::kBoxCols, (j + kL2PrefetchTiles) * kBN, h, b, p.bshd);
           }
 #pragma unroll
         for (int kind = 0; kind < 2; ++kind) {
@@ -361,9 +375,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* dst = s_kv + st * C::kTileBytes;
           mbar_arrive_expect_tx(&ctl->kv_full[st], C::kTileBytes);
           const CUtensorMap* map = kind == 0 ? &tm_k : &tm_v;
-          for (int x = 0; x < D / 64; ++x)
-            load_box(dst + x * (kBN * 128), map, &ctl->kv_full[st], x * 64, j * kBN, h, b,
-                     p.bshd);
+          for (int x = 0; x < C::kBoxes; ++x)
+            load_box(dst + x * (kBN * 128), map, &ctl->kv_full[st], x * C::kBoxCols, j * kBN,
+                     h, b, p.bshd);
           issued = idx + 1;
         }
       }
@@ -378,8 +392,10 @@ __global__ void __launch_bounds__(kThreads, 1)
    } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n_all > 0) {
-      constexpr uint32_t id_s = idesc_f16(kBF16, kBM, kBN, false, false);
-      constexpr uint32_t id_o = idesc_f16(kBF16, kBM, D, false, true);
+      constexpr uint32_t id_s =
+          kFp8 ? idesc_e4m3(kBM, kBN, false, false) : idesc_f16(kBF16, kBM, kBN, false, false);
+      constexpr uint32_t id_o =
+          kFp8 ? idesc_e4m3(kBM, D, false, true) : idesc_f16(kBF16, kBM, D, false, true);
       const uint32_t q_addr = smem_u32(s_q);
       const uint32_t kv_addr = smem_u32(s_kv);
       bool ok = true;
@@ -393,7 +409,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t hi_k = sdesc_hi_sw128(1024);  // K-major: 8-row groups 1024 B apart
       const uint32_t q_lo = sdesc_lo(q_addr, 16);
       const uint32_t k_lo = sdesc_lo(kv_addr, 16);         // K-major: leading offset unused
-      const uint32_t v_lo = sdesc_lo(kv_addr, kBN * 128);  // V: 64-column groups 16 KB apart
+      // V: 128-byte column groups 16 KB apart (FP8, D = 128: a single group)
+      const uint32_t v_lo = sdesc_lo(kv_addr, kBN * 128);
       constexpr uint32_t kTileLo = C::kTileBytes >> 4;
       // S_t = Q_t K_j^T  (both operands K-major, 128-byte swizzle)
       auto issue_s = [&](int t, int st) {
@@ -401,22 +418,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ka = k_lo + st * kTileLo;
         const uint32_t d = tmem + C::col_s(t);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < D * C::kElt / 32; ++kk) {  // 32 bytes of K per instruction
           const uint32_t off = ((kk / 4) * (kBM * 128) + (kk % 4) * 32) >> 4;
-          mma_ss_lh(d, qa + off, hi_k, ka + off, hi_k, id_s, kk > 0);
+          mma_ss_lh<kFp8>(d, qa + off, hi_k, ka + off, hi_k, id_s, kk > 0);
         }
       };
       // O_t (+)= P_t V_j  (P from tensor memory, V MN-major, 128-byte swizzle)
-      // Half `hf` covers keys [64*hf, 64*hf + 64): P columns [32*hf, 32*hf + 32).
+      // Half `hf` covers keys [64*hf, 64*hf + 64); every instruction reads 8
+      // tensor-memory columns of P (16 keys as 16-bit pairs, 32 as E4M3 quads).
       auto issue_pv_half = [&](int t, int st, bool acc, int hf) {
         const uint32_t va = v_lo + st * kTileLo;
         const uint32_t d = tmem + C::col_o(t);
         const uint32_t a = tmem + C::col_s(t);
+        constexpr int kPerHalf = 64 / C::kKeysPerPV;
 #pragma unroll
-        for (int k4 = 0; k4 < kBN / 32; ++k4) {
-          const int kk = hf * (kBN / 32) + k4;
-          mma_ts_lh(d, a + kk * 8, va + ((kk * 16 * 128) >> 4), hi_k, id_o,
-                    (acc || kk > 0) ? 1u : 0u);
+        for (int k4 = 0; k4 < kPerHalf; ++k4) {
+          const int kk = hf * kPerHalf + k4;
+          mma_ts_lh<kFp8>(d, a + kk * 8, va + ((kk * C::kKeysPerPV * 128) >> 4), hi_k, id_o,
+                          (acc || kk > 0) ? 1u : 0u);
         }
       };
       // A K/V stage is free once this CTA's MMAs (and the partner's) read it.
@@ -553,21 +572,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        uint32_t pk[32];
+        if constexpr (kFp8) {
+          uint32_t pk[16];  // 64 keys as E4M3, four per column
 #pragma unroll
-        for (int q = 0; q < 32; ++q) {
-          float x0, x1;
-          f2_unpack(f2_fma(f2_pack(s[half * 64 + 2 * q], s[half * 64 + 2 * q + 1]), c2, nm2), x0,
-                    x1);
-          const float e0 = ex2_approx(x0);
-          const float e1 = ex2_approx(x1);
-          if (q & 1)
-            acc1 = f2_add(acc1, f2_pack(e0, e1));
-          else
+          for (int q = 0; q < 16; ++q) {
+            float x0, x1, x2, x3;
+            f2_unpack(f2_fma(f2_pack(s[half * 64 + 4 * q], s[half * 64 + 4 * q + 1]), c2, nm2),
+                      x0, x1);
+            f2_unpack(f2_fma(f2_pack(s[half * 64 + 4 * q + 2], s[half * 64 + 4 * q + 3]), c2,
+                             nm2),
+                      x2, x3);
+            const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
+            const float e2 = ex2_approx(x2), e3 = ex2_approx(x3);
             acc0 = f2_add(acc0, f2_pack(e0, e1));
-          pk[q] = pack2<kBF16>(e0, e1);
+            acc1 = f2_add(acc1, f2_pack(e2, e3));
+            pk[q] = pack4_e4m3(e0, e1, e2, e3);
+          }
+          tmem_st16(lane_addr + col_s + half * 16, pk);
+        } else {
+          uint32_t pk[32];
+#pragma unroll
+          for (int q = 0; q < 32; ++q) {
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(s[half * 64 + 2 * q], s[half * 64 + 2 * q + 1]), c2, nm2),
+                      x0, x1);
+            const float e0 = ex2_approx(x0);
+            const float e1 = ex2_approx(x1);
+            if (q & 1)
+              acc1 = f2_add(acc1, f2_pack(e0, e1));
+            else
+              acc0 = f2_add(acc0, f2_pack(e0, e1));
+            pk[q] = pack2<kBF16>(e0, e1);
+          }
+          tmem_st32(lane_addr + col_s + half * 32, pk);
         }
-        tmem_st32(lane_addr + col_s + half * 32, pk);
         tmem_st_wait();
         tc_fence_before_sync();
         __syncwarp();
@@ -584,8 +622,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&ctl->o_full, 0, p.wait_limit_ns, p.err, 40 + t));
     tc_fence_after_sync();
     const bool have_o = ok && n_kv(t) > 0 && l > 0.f;
-    const float inv_l = have_o ? 1.f / l : 0.f;
-    uint8_t* s_o = s_q + t * C::kTileBytes;  // Q_t is dead once o_full fired
+    const float inv_l = have_o ? p.o_scale / l : 0.f;
+    // 16-bit inputs: Q_t is dead once o_full fired and holds O_t; FP8: O has
+    // its own tiles.
+    uint8_t* s_o = kFp8 ? smem + C::kOStageOff + t * C::kOTileBytes : s_q + t * C::kTileBytes;
 #pragma unroll 1
     for (int cc = 0; cc < D; cc += 64) {
       uint32_t o[64] = {};
@@ -630,11 +670,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-template <int D, bool kBF16, bool kPaged>
+template <int D, bool kBF16, bool kPaged, bool kFp8 = false>
 static cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                               const CUtensorMap& o, const PrefillParams& p, int grid,
                               cudaStream_t stream) {
-  auto kern = prefill_fwd_kernel<D, kBF16, kPaged>;
+  auto kern = prefill_fwd_kernel<D, kBF16, kPaged, kFp8>;
   static bool configured = false;  // per template instance
   if (!configured) {
     // The in-kernel register split assumes exactly kRegsAtLaunch registers
@@ -644,18 +684,18 @@ static cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const 
     if (e != cudaSuccess) return e;
     if (fa.numRegs != kRegsAtLaunch) return cudaErrorInvalidConfiguration;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg<D>::kSmemBytes);
+                             Cfg<D, kFp8>::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   if (!(kPaged && p.pair)) {
-    kern<<<grid, kThreads, Cfg<D>::kSmemBytes, stream>>>(q, k, v, o, p);
+    kern<<<grid, kThreads, Cfg<D, kFp8>::kSmemBytes, stream>>>(q, k, v, o, p);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Cfg<D>::kSmemBytes;
+  cfg.dynamicSmemBytes = Cfg<D, kFp8>::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -687,6 +727,15 @@ cudaError_t extend_launch(const CUtensorMap& q, const CUtensorMap& k, const CUte
                             : launch_one<128, false, true>(q, k, v, o, p, grid, stream);
   return bf16 ? launch_one<64, true, true>(q, k, v, o, p, grid, stream)
               : launch_one<64, false, true>(q, k, v, o, p, grid, stream);
+}
+
+cudaError_t prefill_fp8_launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                               const CUtensorMap& o, const PrefillParams& p, bool bf16_out,
+                               cudaStream_t stream) {
+  const int grid = p.B * p.H * p.num_q_blocks;
+  if (grid == 0) return cudaSuccess;
+  return bf16_out ? launch_one<128, true, false, true>(q, k, v, o, p, grid, stream)
+                  : launch_one<128, false, false, true>(q, k, v, o, p, grid, stream);
 }
 
 int prefill_rows_per_cta() { return kTiles * kBM; }

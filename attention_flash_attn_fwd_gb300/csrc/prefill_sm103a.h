@@ -26,6 +26,7 @@ struct PrefillParams {
   const void* k_pool;         // [num_pages, page_size, H_kv, D]
   const void* v_pool;
   int pair;                   // 1: CTA pairs (clusters of 2) share K/V tiles; needs an even group
+  float o_scale;              // multiplies O at the end (the FP8 form's V descale, else 1)
 };
 
 // Tensor maps: 16-bit elements, 128-byte swizzle, box = 64 columns x
@@ -40,6 +41,12 @@ cudaError_t prefill_launch(const CUtensorMap& q, const CUtensorMap& k, const CUt
 cudaError_t extend_launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                           const CUtensorMap& o, const PrefillParams& p, int D, bool bf16,
                           cudaStream_t stream);
+
+// FP8 form (D = 128 only): q/k/v maps over E4M3 bytes, box 128 columns x
+// prefill_box_rows() rows; o map 16-bit as for prefill.
+cudaError_t prefill_fp8_launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                               const CUtensorMap& o, const PrefillParams& p, bool bf16_out,
+                               cudaStream_t stream);
 
 int prefill_rows_per_cta();
 int prefill_box_rows();

@@ -55,4 +55,27 @@ inline bool encode_tiled_16bit(CUtensorMap* map, const void* base, int rank,
   return r == CUDA_SUCCESS;
 }
 
+// Same for a tensor of 8-bit codes (E4M3 bytes are moved as UINT8).
+inline bool encode_tiled_8bit(CUtensorMap* map, const void* base, int rank,
+                              const uint64_t* dims, const uint64_t* strides_bytes,
+                              const uint32_t* box, CUtensorMapSwizzle swizzle,
+                              CUtensorMapL2promotion promo = CU_TENSOR_MAP_L2_PROMOTION_L2_256B) {
+  EncodeTiledFn enc = get_encode_tiled();
+  if (!enc) return false;
+  cuuint64_t d[5];
+  cuuint64_t s[4];
+  cuuint32_t b[5];
+  cuuint32_t e[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    e[i] = 1;
+  }
+  for (int i = 0; i < rank - 1; ++i) s[i] = strides_bytes[i];
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<cuuint32_t>(rank),
+                   const_cast<void*>(base), d, s, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                   promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace attn_host

@@ -83,6 +83,31 @@ ATTN_API attn_status attn_prefill_fwd(const void* q, const void* k, const void* 
                              attn_dtype dtype, int causal, float scale, cudaStream_t stream);
 
 /*
+ * FP8 prefill attention forward: the prefill operation on E4M3 inputs.
+ *
+ * Defines: attn_prefill_fwd's O and lse for Q = descale_q * q, K = descale_k *
+ * k, V = descale_v * v, where q, k, v hold OCP 8-bit E4M3 codes (the layout
+ * of torch.float8_e4m3fn) ("FAv3 - FP8", Wave February 2025 Release,
+ * FlashDecoding list).
+ *
+ *   q, k, v    E4M3 bytes, [B,H,S,D] (ATTN_BHSD) or [B,S,H,D] (ATTN_BSHD)
+ *   o          output in out_dtype (ATTN_F16 or ATTN_BF16), q's shape and layout
+ *   lse        [B,H,S_q] fp32 natural-log row sums of the real scores, or NULL
+ *   descale_*  per-tensor factors, finite and > 0
+ *   D          128 only (else ATTN_ERR_UNSUPPORTED); other arguments as for
+ *              attn_prefill_fwd.
+ * Both products run on E4M3 operands with fp32 accumulation; P is rounded to
+ * E4M3 (relative error up to 2^-4 per weight) before P V, which sets the
+ * accuracy: about 2-3% relative L2 error on O for N(0,1) inputs, independent
+ * of the sequence length.
+ */
+ATTN_API attn_status attn_prefill_fp8_fwd(const void* q, const void* k, const void* v, void* o,
+                                          float* lse, int B, int H, int S_q, int S_kv, int D,
+                                          attn_layout layout, attn_dtype out_dtype, int causal,
+                                          float scale, float descale_q, float descale_k,
+                                          float descale_v, cudaStream_t stream);
+
+/*
  * Extend attention forward: prefill of S_q new tokens per sequence against the
  * sequence's cached keys in a paged KV pool (prefix-cached / chunked prefill).
  *
@@ -149,9 +174,11 @@ ATTN_API attn_status attn_extend_fwd(const void* q, const void* k_pool, const vo
  *   scale      softmax scale, finite and > 0.
  *   dtype      ATTN_F16 or ATTN_BF16 (ADDED: not in the published signature).
  *   H_q % H_kv == 0, H_q / H_kv <= 16, D == 128 (else ATTN_ERR_UNSUPPORTED).
- * The library owns a split-partials workspace, grown on demand outside stream
- * capture; growing it during capture returns ATTN_ERR_NO_MEMORY (call once
- * with the largest shapes before capturing).
+ * The library owns a split-partials workspace per (device, stream), grown on
+ * demand outside stream capture; growing it during capture returns
+ * ATTN_ERR_NO_MEMORY (call once with the largest shapes before capturing).
+ * Calls on different streams may run concurrently; calls on one stream use
+ * its workspace in stream order.
  */
 ATTN_API attn_status attn_decode_fwd(const void* q, const void* k_pool, const void* v_pool,
                             const int32_t* page_table, const int32_t* kv_lens, void* o, int B,
@@ -205,7 +232,8 @@ ATTN_API attn_status attn_device_error(int* word, int clear);
  */
 ATTN_API void attn_set_wait_limit_ns(uint64_t ns);
 
-/* Free the decode workspace of the current device (not during capture). */
+/* Free the decode workspaces (all streams) of the current device; synchronizes
+ * the device (not during capture). */
 ATTN_API attn_status attn_release_workspace(void);
 
 /* Library version string. */

@@ -11,6 +11,17 @@ MAX_ABS = 2e-2
 REL_L2 = 5e-3
 LSE_ABS = 1e-3
 
+# FP8 (E4M3) prefill.  The kernel must round P to E4M3 before P V; with 3
+# mantissa bits the rounding error of each weight is up to 2^-4 relative
+# (rms about 2^-4/sqrt(3) for round-to-nearest), the errors of different keys
+# are independent and O = sum_j w_j v_j, so for N(0,1) V the relative L2 error
+# of O is about rms(delta) ~ 2-3% at every sequence length (a CPU emulation
+# of this rounding gave 1.9-2.7% for S = 128 .. 4096); early causal rows, where
+# O is a few V rows of size ~1, reach ~3.5e-2 absolute.  The bounds leave a
+# 1.5x / 3x margin.  The scores and lse are not rounded through E4M3.
+FP8_MAX_ABS = 1e-1
+FP8_REL_L2 = 4e-2
+
 
 def errors(out, ref):
     """(max_abs, rel_l2) of a GPU output against a float64 reference."""
@@ -23,10 +34,11 @@ def errors(out, ref):
     return max_abs, rel
 
 
-def assert_close(out, ref, what=""):
+def assert_close(out, ref, what="", max_abs_tol=MAX_ABS, rel_tol=REL_L2):
     max_abs, rel = errors(out, ref)
-    assert max_abs <= MAX_ABS and rel <= REL_L2, (
-        "%s: max_abs=%.3e (<= %.0e) rel_l2=%.3e (<= %.0e)" % (what, max_abs, MAX_ABS, rel, REL_L2))
+    assert max_abs <= max_abs_tol and rel <= rel_tol, (
+        "%s: max_abs=%.3e (<= %.0e) rel_l2=%.3e (<= %.0e)" % (what, max_abs, max_abs_tol, rel,
+                                                              rel_tol))
     return max_abs, rel
 
 

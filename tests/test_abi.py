@@ -111,6 +111,36 @@ def test_decode_empty_batch_is_a_no_op():
     assert _decode(B=0, num_pages=0) == attn.ATTN_OK
 
 
+def _prefill_fp8(**kw):
+    a = dict(q=16, k=16, v=16, o=16, lse=None, B=1, H=1, S_q=8, S_kv=8, D=128, layout=0,
+             out_dtype=1, causal=0, scale=0.1, descale_q=1.0, descale_k=1.0, descale_v=1.0,
+             stream=None)
+    a.update(kw)
+    return attn.attn_prefill_fp8_fwd(**a)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(D=64), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(layout=3), attn.ATTN_ERR_INVALID_ARG),
+    (dict(out_dtype=4), attn.ATTN_ERR_INVALID_ARG),
+    (dict(causal=-1), attn.ATTN_ERR_INVALID_ARG),
+    (dict(descale_q=0.0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(descale_v=float("nan")), attn.ATTN_ERR_INVALID_ARG),
+    (dict(descale_k=-2.0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=0.0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(q=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(k=4), attn.ATTN_ERR_INVALID_ARG),  # misaligned
+])
+def test_prefill_fp8_rejects_bad_arguments(kw, code):
+    assert _prefill_fp8(**kw) == code
+    assert attn.attn_last_error()
+
+
+def test_prefill_fp8_empty_problem_is_a_no_op():
+    assert _prefill_fp8(B=0, q=None, k=None, v=None, o=None) == attn.ATTN_OK
+    assert _prefill_fp8(S_q=0) == attn.ATTN_OK
+
+
 def _extend(**kw):
     a = dict(q=16, k_pool=16, v_pool=16, page_table=16, kv_lens=16, o=16, lse=None, B=2, S_q=64,
              H_q=8, H_kv=2, D=128, page_size=16, max_pages_per_seq=8, num_pages=16, dtype=1,

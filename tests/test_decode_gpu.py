@@ -167,3 +167,27 @@ def test_full_size_paged_sampled(paged_full):
     lens = inp.kv_lens.tolist()
     bs = sorted({1, lens.index(max(lens)), lens.index(min(lens)), 30})
     _check_sampled(inp, out, bs, workloads.C5.scale)
+
+
+def test_decode_concurrent_streams_do_not_share_partials():
+    """Two decode calls on different streams, launched back to back so their
+    kernels can overlap: each stream has its own split workspace, so each
+    result equals the same call made alone."""
+    case = workloads.DecodeCase("t", 8, 32, 8, 128, 2000, 8000, 8192, paged=True, seed=9)
+    a = workloads.make_decode(case)
+    b = workloads.make_decode(workloads.DecodeCase("t", 8, 32, 8, 128, 2000, 8000, 8192,
+                                                   paged=True, seed=10))
+    dev = [[t.cuda() for t in (x.q, x.k, x.v, x.kv_lens, x.page_table)] for x in (a, b)]
+    alone = []
+    for q, k, v, lens, pt in dev:
+        alone.append(attn.decode(q, k, v, lens, page_table=pt, scale=case.scale))
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    outs = [torch.empty_like(dev[0][0]), torch.empty_like(dev[1][0])]
+    for _ in range(20):
+        for (q, k, v, lens, pt), o, s in zip(dev, outs, (s1, s2)):
+            with torch.cuda.stream(s):
+                attn.decode(q, k, v, lens, page_table=pt, scale=case.scale, out=o)
+    torch.cuda.synchronize()
+    assert attn.attn_device_error() == 0
+    assert torch.equal(outs[0], alone[0]) and torch.equal(outs[1], alone[1])

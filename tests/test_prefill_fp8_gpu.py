@@ -1,0 +1,104 @@
+"""FP8 (E4M3) prefill parity against the float64 oracle, through the C ABI.
+
+Tolerances are the FP8 bounds of parity.py (derived there from the E4M3
+rounding of P)."""
+import numpy as np
+import pytest
+import torch
+
+import attention_flash_attn_fwd_gb300 as attn
+import oracle
+import workloads
+from parity import FP8_MAX_ABS, FP8_REL_L2, assert_close, assert_lse_close, errors
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(case, out_dtype=torch.bfloat16):
+    q8, k8, v8, dq, dk, dv = workloads.make_prefill_fp8(case)
+    o, lse = attn.prefill_fp8(q8.cuda(), k8.cuda(), v8.cuda(), descale_q=dq, descale_k=dk,
+                              descale_v=dv, causal=case.causal, scale=case.scale,
+                              layout=case.layout, out_dtype=out_dtype, return_lse=True)
+    torch.cuda.synchronize()
+    assert attn.attn_device_error() == 0
+    return (q8, k8, v8, dq, dk, dv), o.cpu(), lse.cpu()
+
+
+def _ref(inputs, case):
+    q8, k8, v8, dq, dk, dv = inputs
+    return oracle.prefill_fp8(q8, k8, v8, descale_q=dq, descale_k=dk, descale_v=dv,
+                              causal=case.causal, scale=case.scale,
+                              layout=oracle.BHSD if case.layout == "bhsd" else oracle.BSHD)
+
+
+@pytest.mark.parametrize("layout", ["bhsd", "bshd"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,S_q,S_kv", [(1, 2, 128, 128), (2, 3, 200, 333), (1, 2, 512, 77),
+                                          (1, 1, 700, 700), (2, 2, 1, 300)])
+def test_prefill_fp8_matches_oracle(B, H, S_q, S_kv, causal, layout):
+    case = workloads.Fp8PrefillCase("t", B, H, S_q, S_kv, 128, layout, causal, seed=41)
+    inputs, o, lse = _run(case)
+    ref_o, ref_lse = _ref(inputs, case)
+    assert_close(o, ref_o, "fp8 %s" % (case,), FP8_MAX_ABS, FP8_REL_L2)
+    assert_lse_close(lse, ref_lse, "fp8 lse %s" % (case,))
+
+
+def test_prefill_fp8_fp16_output():
+    case = workloads.Fp8PrefillCase("t", 2, 2, 300, 300, 128, "bhsd", True, seed=42)
+    inputs, o, lse = _run(case, out_dtype=torch.float16)
+    assert o.dtype == torch.float16
+    ref_o, _ = _ref(inputs, case)
+    assert_close(o, ref_o, "fp8 fp16-out", FP8_MAX_ABS, FP8_REL_L2)
+
+
+def test_prefill_fp8_error_is_p_rounding_not_worse():
+    """The measured error stays near the derived E4M3-of-P level (2-3%), well
+    inside the bound, on a long non-causal case."""
+    case = workloads.Fp8PrefillCase("t", 1, 4, 1024, 2048, 128, "bhsd", False, seed=43)
+    inputs, o, _ = _run(case)
+    ref_o, _ = _ref(inputs, case)
+    _, rel = errors(o, ref_o)
+    assert 5e-3 < rel < 3.5e-2, rel
+
+
+def test_prefill_fp8_descale_factors_apply():
+    """Scaling the V descale scales O; scaling Q's descale is the same as
+    scaling the softmax scale."""
+    case = workloads.Fp8PrefillCase("t", 1, 2, 256, 256, 128, "bhsd", False, seed=44)
+    q8, k8, v8, dq, dk, dv = workloads.make_prefill_fp8(case)
+    args = [t.cuda() for t in (q8, k8, v8)]
+    o1 = attn.prefill_fp8(*args, descale_q=dq, descale_k=dk, descale_v=dv, scale=case.scale)
+    o2 = attn.prefill_fp8(*args, descale_q=dq, descale_k=dk, descale_v=2 * dv, scale=case.scale)
+    o3 = attn.prefill_fp8(*args, descale_q=2 * dq, descale_k=dk, descale_v=dv, scale=case.scale)
+    o4 = attn.prefill_fp8(*args, descale_q=dq, descale_k=dk, descale_v=dv, scale=2 * case.scale)
+    torch.cuda.synchronize()
+    torch.testing.assert_close(o2.float(), 2 * o1.float(), rtol=1e-2, atol=1e-3)
+    assert torch.equal(o3, o4)
+
+
+def test_prefill_fp8_empty_kv_and_determinism():
+    case = workloads.Fp8PrefillCase("t", 1, 2, 300, 600, 128, "bshd", True, seed=45)
+    inputs, o1, l1 = _run(case)
+    _, o2, l2 = _run(case)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    q8 = inputs[0].cuda()
+    o, lse = attn.prefill_fp8(q8, q8[:, :0], q8[:, :0], descale_q=1.0, descale_k=1.0,
+                              descale_v=1.0, layout="bshd", return_lse=True)
+    torch.cuda.synchronize()
+    assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
+
+
+@pytest.mark.parametrize("case", [workloads.C7, workloads.C7_CAUSAL], ids=lambda c: c.name)
+def test_prefill_fp8_full_size_sampled_heads(case):
+    inputs, o, lse = _run(case)
+    q8, k8, v8, dq, dk, dv = inputs
+    g = torch.Generator().manual_seed(46)
+    for _ in range(3):
+        b = int(torch.randint(case.B, (1,), generator=g))
+        h = int(torch.randint(case.H, (1,), generator=g))
+        sl = lambda x: x[b:b + 1, h:h + 1]
+        ref_o, ref_lse = oracle.prefill_fp8(sl(q8), sl(k8), sl(v8), descale_q=dq, descale_k=dk,
+                                            descale_v=dv, causal=case.causal, scale=case.scale)
+        assert_close(o[b:b + 1, h:h + 1], ref_o, "%s b=%d h=%d" % (case.name, b, h), FP8_MAX_ABS,
+                     FP8_REL_L2)
+        assert_lse_close(lse[b:b + 1, h:h + 1], ref_lse, "%s lse" % case.name)
