@@ -44,9 +44,9 @@
 // issues every other page box multicast to both, and each MMA warp releases
 // a K/V stage in both CTAs (0.96 -> 0.80 ms with 16-token pages).
 //
-// The FP8 form (kFp8; Wave February 2025 Release, "FAv3 - FP8") reads E4M3
-// Q, K, V: tiles are half the bytes (one 128-byte swizzled panel holds a
-// 128-wide row), both products run as `.kind::f8f6f4` MMAs (K = 32 per
+// The FP8 form (kFp8; Wave February 2025 Release, EvoFormer list, "FAv3 -
+// FP8") reads E4M3 Q, K, V: tiles are half the bytes (one 128-byte swizzled
+// panel holds a 128-wide row), both products run as `.kind::f8f6f4` MMAs (K = 32 per
 // instruction), P is written to tensor memory as E4M3 (four per column) and
 // the per-tensor descale factors fold into the softmax scale and the final
 // 1/l.  O (bf16 or fp16) is staged in its own shared-memory tiles.

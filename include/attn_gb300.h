@@ -88,7 +88,7 @@ ATTN_API attn_status attn_prefill_fwd(const void* q, const void* k, const void* 
  * Defines: attn_prefill_fwd's O and lse for Q = descale_q * q, K = descale_k *
  * k, V = descale_v * v, where q, k, v hold OCP 8-bit E4M3 codes (the layout
  * of torch.float8_e4m3fn) ("FAv3 - FP8", Wave February 2025 Release,
- * FlashDecoding list).
+ * EvoFormer list).
  *
  *   q, k, v    E4M3 bytes, [B,H,S,D] (ATTN_BHSD) or [B,S,H,D] (ATTN_BSHD)
  *   o          output in out_dtype (ATTN_F16 or ATTN_BF16), q's shape and layout

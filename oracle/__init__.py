@@ -22,8 +22,10 @@ are stated at the top of ``attn_oracle.c``:
   paged pool, bottom-right causal per sequence (Wave February 2025 Release,
   "Extend Attention"; WAVE MLSys 2026 summary, Integration: SGLang extend);
 * FP8 prefill: the prefill definition on E4M3 codes times per-tensor descale
-  factors (Wave February 2025 Release, "FAv3 - FP8"), E4M3 decoded from the
-  OCP 8-bit floating point definition.
+  factors (Wave February 2025 Release, EvoFormer list, "FAv3 - FP8"), E4M3 decoded from the
+  OCP 8-bit floating point definition;
+* backward: dQ, dK, dV of the prefill definition by the chain rule
+  (Wave February 2025 Release, EvoFormer list, "Backward Flash Attention").
 
 Every function here is pinned by ``tests/test_oracle.py`` against library
 routines, closed forms and analytic fixtures; no part is left unpinned.
@@ -87,6 +89,10 @@ def _load():
             lib.oracle_extend_f64.restype = ctypes.c_int
             lib.oracle_e4m3_decode.argtypes = [ctypes.POINTER(ctypes.c_uint8), dp, L]
             lib.oracle_e4m3_decode.restype = None
+            lib.oracle_prefill_bwd_f64.argtypes = [dp, dp, dp, dp, dp, dp, dp, L, L, L, L, L,
+                                                   ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                                   ctypes.c_int]
+            lib.oracle_prefill_bwd_f64.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -238,3 +244,30 @@ def prefill_fp8(q, k, v, *, descale_q: float, descale_k: float, descale_v: float
     return prefill(decode_e4m3(q) * float(descale_q), decode_e4m3(k) * float(descale_k),
                    decode_e4m3(v) * float(descale_v), causal=causal, scale=scale, layout=layout,
                    n_threads=n_threads)
+
+
+def prefill_bwd(q, k, v, dout, *, causal: bool, scale: float, layout: int = BHSD,
+                n_threads: int | None = None):
+    """Gradients (dq, dk, dv) in float64 of ``O = prefill(q, k, v)`` for the
+    upstream gradient ``dout`` (q's shape); layouts as ``prefill``."""
+    q64, k64, v64, do64 = _f64(q), _f64(k), _f64(v), _f64(dout)
+    if layout == BHSD:
+        B, H, S_q, D = q64.shape
+        S_kv = k64.shape[2]
+    elif layout == BSHD:
+        B, S_q, H, D = q64.shape
+        S_kv = k64.shape[1]
+    else:
+        raise ValueError("layout must be BHSD (0) or BSHD (1)")
+    if do64.shape != q64.shape or k64.shape != v64.shape:
+        raise ValueError("shape mismatch")
+    dq = np.zeros(q64.shape, dtype=np.float64)
+    dk = np.zeros(k64.shape, dtype=np.float64)
+    dv = np.zeros(v64.shape, dtype=np.float64)
+    rc = _load().oracle_prefill_bwd_f64(_dptr(q64), _dptr(k64), _dptr(v64), _dptr(do64),
+                                        _dptr(dq), _dptr(dk), _dptr(dv), B, H, S_q, S_kv, D,
+                                        int(layout), int(bool(causal)), float(scale),
+                                        int(n_threads or default_threads()))
+    if rc != 0:
+        raise RuntimeError("oracle_prefill_bwd_f64 failed (rc=%d)" % rc)
+    return dq, dk, dv

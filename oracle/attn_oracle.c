@@ -46,13 +46,23 @@
  * its kv_lens[b] cached keys (which include the new tokens), causal
  * alignment bottom-right per sequence, kv head h / (H_q / H_kv).
  *
- * FP8 prefill ("FAv3 - FP8", Wave February 2025 Release, FlashDecoding list)
+ * FP8 prefill ("FAv3 - FP8", Wave February 2025 Release, EvoFormer list)
  * is the same definition on inputs stored as 8-bit E4M3 codes with one
  * descale factor per tensor: x = descale * value(code).  value() follows the
  * OCP 8-bit floating point E4M3 format: sign bit, 4 exponent bits with bias
  * 7, 3 mantissa bits; exponent 0 encodes subnormals m/8 * 2^-6; the all-ones
  * exponent with all-ones mantissa is NaN; there is no infinity (so the
  * largest finite value is 1.75 * 2^8 = 448).
+ *
+ * Backward ("Backward Flash Attention", Wave February 2025 Release,
+ * EvoFormer list; "Functionality & Performance on backward attention",
+ * Milestones): the gradients of the same
+ * definition, written out from the chain rule with P the exact softmax,
+ *     O_i   = sum_j P_ij v_j,          D_i = sum_d dO_i[d] O_i[d]
+ *     dV_j  = sum_i P_ij dO_i,         dP_ij = dO_i . v_j
+ *     dS_ij = P_ij (dP_ij - D_i)
+ *     dQ_i  = scale sum_j dS_ij k_j,   dK_j = scale sum_i dS_ij q_i
+ * over the visible (i, j) pairs.
  *
  * Rows are independent; they are spread over POSIX threads.
  */
@@ -382,4 +392,98 @@ void oracle_e4m3_decode(const uint8_t *in, double *out, long n) {
             v = ldexp(1.0 + (double)m / 8.0, e - 7);
         out[i] = sign ? -v : v;
     }
+}
+
+/* --------------------------------------------------------------- backward */
+
+typedef struct {
+    const double *q, *k, *v, *dout;
+    double *dq, *dk, *dv;
+    long B, H, S_q, S_kv, D;
+    int layout, causal;
+    double scale;
+    long next_head; /* shared work counter over (b, h) */
+} bwd_job;
+
+static void *bwd_worker(void *arg) {
+    bwd_job *J = (bwd_job *)arg;
+    const long D = J->D, S_kv = J->S_kv;
+    double *p = (double *)malloc(sizeof(double) * (size_t)(S_kv + 1));
+    double *o = (double *)malloc(sizeof(double) * (size_t)(D + 1));
+    if (!p || !o) { free(p); free(o); return (void *)1; }
+    const long total = J->B * J->H;
+    for (;;) {
+        long r = __atomic_fetch_add(&J->next_head, 1, __ATOMIC_RELAXED);
+        if (r >= total) break;
+        const long b = r / J->H, h = r % J->H;
+        /* this head's dK and dV start at zero; dQ rows are written whole */
+        for (long j = 0; j < S_kv; ++j)
+            for (long d = 0; d < D; ++d) {
+                J->dk[offset4(J->layout, b, h, j, d, J->H, S_kv, D)] = 0.0;
+                J->dv[offset4(J->layout, b, h, j, d, J->H, S_kv, D)] = 0.0;
+            }
+        for (long i = 0; i < J->S_q; ++i) {
+            const double *q_row = J->q + offset4(J->layout, b, h, i, 0, J->H, J->S_q, D);
+            const double *do_row = J->dout + offset4(J->layout, b, h, i, 0, J->H, J->S_q, D);
+            double *dq_row = J->dq + offset4(J->layout, b, h, i, 0, J->H, J->S_q, D);
+            for (long d = 0; d < D; ++d) dq_row[d] = 0.0;
+            long last = S_kv - 1;
+            if (J->causal) {
+                long lim = i + (S_kv - J->S_q);
+                if (lim < last) last = lim;
+            }
+            if (last < 0) continue; /* no visible key: O_i = 0, no gradient */
+            /* P_i by the definition */
+            double m = -INFINITY;
+            for (long j = 0; j <= last; ++j) {
+                const double *k_row = J->k + offset4(J->layout, b, h, j, 0, J->H, S_kv, D);
+                double dot = 0.0;
+                for (long d = 0; d < D; ++d) dot += q_row[d] * k_row[d];
+                p[j] = J->scale * dot;
+                if (p[j] > m) m = p[j];
+            }
+            double l = 0.0;
+            for (long j = 0; j <= last; ++j) { p[j] = exp(p[j] - m); l += p[j]; }
+            for (long j = 0; j <= last; ++j) p[j] /= l;
+            /* O_i and D_i */
+            for (long d = 0; d < D; ++d) o[d] = 0.0;
+            for (long j = 0; j <= last; ++j) {
+                const double *v_row = J->v + offset4(J->layout, b, h, j, 0, J->H, S_kv, D);
+                for (long d = 0; d < D; ++d) o[d] += p[j] * v_row[d];
+            }
+            double Di = 0.0;
+            for (long d = 0; d < D; ++d) Di += do_row[d] * o[d];
+            for (long j = 0; j <= last; ++j) {
+                const double *k_row = J->k + offset4(J->layout, b, h, j, 0, J->H, S_kv, D);
+                const double *v_row = J->v + offset4(J->layout, b, h, j, 0, J->H, S_kv, D);
+                double *dk_row = J->dk + offset4(J->layout, b, h, j, 0, J->H, S_kv, D);
+                double *dv_row = J->dv + offset4(J->layout, b, h, j, 0, J->H, S_kv, D);
+                double dp = 0.0;
+                for (long d = 0; d < D; ++d) dp += do_row[d] * v_row[d];
+                const double ds = p[j] * (dp - Di);
+                for (long d = 0; d < D; ++d) {
+                    dv_row[d] += p[j] * do_row[d];
+                    dq_row[d] += J->scale * ds * k_row[d];
+                    dk_row[d] += J->scale * ds * q_row[d];
+                }
+            }
+        }
+    }
+    free(p);
+    free(o);
+    return NULL;
+}
+
+/* Gradients of O = softmax(scale Q K^T + mask) V for the upstream gradient
+ * dout (q's shape).  q, dout, dq: [B,H,S_q,D] or [B,S_q,H,D]; k, v, dk, dv:
+ * the same layout with S_kv.  Returns 0, or -1 on bad arguments. */
+int oracle_prefill_bwd_f64(const double *q, const double *k, const double *v,
+                           const double *dout, double *dq, double *dk, double *dv,
+                           long B, long H, long S_q, long S_kv, long D, int layout,
+                           int causal, double scale, int n_threads) {
+    if (B < 0 || H < 0 || S_q < 0 || S_kv < 0 || D <= 0) return -1;
+    if (layout != ORACLE_BHSD && layout != ORACLE_BSHD) return -1;
+    if (B == 0 || H == 0) return 0;
+    bwd_job J = {q, k, v, dout, dq, dk, dv, B, H, S_q, S_kv, D, layout, causal, scale, 0};
+    return run_threads(bwd_worker, &J, n_threads);
 }

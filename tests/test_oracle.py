@@ -427,6 +427,81 @@ def test_fp8_quantization_is_within_half_a_step():
     assert rel <= 2.0 ** -4 + 1e-12
 
 
+# --------------------------------------------------------------- backward
+
+
+def _torch_grads(q, k, v, dout, scale, mask):
+    """PyTorch float64 autograd of SDPA on [B,H,S,D] tensors."""
+    q, k, v = (t.detach().clone().requires_grad_(True) for t in (q, k, v))
+    o = F.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=scale)
+    o.backward(dout)
+    return q.grad, k.grad, v.grad
+
+
+@pytest.mark.parametrize("layout", ["bhsd", "bshd"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("S_q,S_kv", [(17, 17), (9, 30), (40, 25)])
+def test_prefill_bwd_matches_torch_autograd(S_q, S_kv, causal, layout):
+    B, H, D = 2, 3, 16
+    q, k, v, do = (_rand((B, H, S, D), sd) for S, sd in ((S_q, 51), (S_kv, 52), (S_kv, 53),
+                                                          (S_q, 54)))
+    mask = _bottom_right(S_q, S_kv) if causal else None
+    if causal and S_q > S_kv:
+        return  # rows with no visible key: PyTorch yields NaN there (covered below)
+    ref = _torch_grads(q, k, v, do, 0.3, mask)
+    tr = (lambda x: x) if layout == "bhsd" else (lambda x: x.transpose(1, 2).contiguous())
+    ours = oracle.prefill_bwd(tr(q), tr(k), tr(v), tr(do), causal=causal, scale=0.3,
+                              layout=oracle.BHSD if layout == "bhsd" else oracle.BSHD)
+    for a, r in zip(ours, ref):
+        torch.testing.assert_close(torch.from_numpy(a), tr(r), rtol=0, atol=TOL)
+
+
+def test_prefill_bwd_matches_finite_differences():
+    """Gradients of L = sum(dout * O) by central differences of the forward
+    oracle, on a tiny causal case (independent of the backward formulas)."""
+    B, H, S_q, S_kv, D = 1, 2, 3, 5, 3
+    q, k, v, do = (_rand((B, H, S, D), sd).numpy() for S, sd in ((S_q, 61), (S_kv, 62),
+                                                                  (S_kv, 63), (S_q, 64)))
+    dq, dk, dv = oracle.prefill_bwd(q, k, v, do, causal=True, scale=0.7, n_threads=1)
+
+    def loss(q_, k_, v_):
+        o, _ = oracle.prefill(q_, k_, v_, causal=True, scale=0.7, n_threads=1)
+        return float((o * do).sum())
+
+    eps = 1e-5
+    for x, g, which in ((q, dq, 0), (k, dk, 1), (v, dv, 2)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            args_p = [q, k, v]
+            args_m = [q, k, v]
+            args_p[which], args_m[which] = xp, xm
+            num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+        np.testing.assert_allclose(g, num, rtol=0, atol=1e-8)
+
+
+def test_prefill_bwd_invariants():
+    """dK sums to zero over the keys of a head (the dS rows sum to zero); a
+    zero upstream gradient gives zero gradients; rows with no visible key
+    (causal, S_q > S_kv) contribute nothing."""
+    B, H, S_q, S_kv, D = 2, 2, 12, 7, 8
+    q, k, v, do = (_rand((B, H, S, D), sd).numpy() for S, sd in ((S_q, 71), (S_kv, 72),
+                                                                  (S_kv, 73), (S_q, 74)))
+    dq, dk, dv = oracle.prefill_bwd(q, k, v, do, causal=False, scale=0.4)
+    np.testing.assert_allclose(dk.sum(axis=2), 0.0, atol=1e-12)
+    z = oracle.prefill_bwd(q, k, v, np.zeros_like(do), causal=False, scale=0.4)
+    assert all(np.all(a == 0.0) for a in z)
+    dq, dk, dv = oracle.prefill_bwd(q, k, v, do, causal=True, scale=0.4)
+    assert np.all(dq[:, :, :S_q - S_kv] == 0.0)  # rows 0..4 see no key
+    do2 = do.copy()
+    do2[:, :, :S_q - S_kv] = 123.0  # their upstream gradient must not matter
+    dq2, dk2, dv2 = oracle.prefill_bwd(q, k, v, do2, causal=True, scale=0.4)
+    np.testing.assert_array_equal(dk, dk2)
+    np.testing.assert_array_equal(dv, dv2)
+
+
 # --------------------------------------------------------- planted mistakes
 
 _MUTANTS = {
@@ -449,6 +524,10 @@ _MUTANTS = {
     "extend_lse_index": ("J->lse + (size_t)((b * J->H_q + h) * J->S_q + i)",
                          "J->lse + (size_t)((b * J->S_q + i) * J->H_q + h)"),
     "v_from_k": ("o_row[d] += w * v_seq[t * D + d];", "o_row[d] += w * k_seq[t * D + d];"),
+    "bwd_dropped_delta": ("const double ds = p[j] * (dp - Di);", "const double ds = p[j] * dp;"),
+    "bwd_dk_from_k": ("dk_row[d] += J->scale * ds * q_row[d];",
+                      "dk_row[d] += J->scale * ds * k_row[d];"),
+    "bwd_dv_from_ds": ("dv_row[d] += p[j] * do_row[d];", "dv_row[d] += ds * do_row[d];"),
     "e4m3_bias_8": ("ldexp(1.0 + (double)m / 8.0, e - 7)", "ldexp(1.0 + (double)m / 8.0, e - 8)"),
     "e4m3_subnormal_as_normal": ("v = ldexp((double)m / 8.0, -6);",
                                  "v = ldexp(1.0 + (double)m / 8.0, -7);"),
@@ -463,6 +542,7 @@ def _pins_pass() -> bool:
         lambda: test_decode_matches_torch_sdpa(True, 8, 2),
         lambda: test_extend_matches_torch_sdpa(True, 8, 2, 8),
         lambda: test_e4m3_decode_matches_torch_for_every_code(),
+        lambda: test_prefill_bwd_matches_torch_autograd(9, 30, True, "bshd"),
     ] + [lambda p=p: test_golden_fixture(p)
          for p in sorted(glob.glob(os.path.join(GOLDEN, "*.json")))]
     for c in checks:
@@ -498,6 +578,8 @@ def test_mutants_are_caught(name):
         mutant.oracle_extend_f64.restype = ctypes.c_int
         mutant.oracle_e4m3_decode.argtypes = saved.oracle_e4m3_decode.argtypes
         mutant.oracle_e4m3_decode.restype = None
+        mutant.oracle_prefill_bwd_f64.argtypes = saved.oracle_prefill_bwd_f64.argtypes
+        mutant.oracle_prefill_bwd_f64.restype = ctypes.c_int
         oracle._lib = mutant
         try:
             assert not _pins_pass(), "pins did not catch planted mistake %r" % name

@@ -19,6 +19,8 @@ Recipe (every draw uses a CPU ``torch.Generator`` seeded with ``seed``):
   data pages placed by the permutation, one extra poison page (all 1e4) is
   appended, unused page-table entries point at it, and page tail slots hold
   1e4 too, so a masking bug is loud but never reads outside the pool.
+* backward: Q, K, V drawn as for prefill, then the upstream gradient dO
+  (q's shape, float32 ``randn`` times ``std``, rounded to the dtype).
 * FP8 prefill: Q, K, V drawn as for prefill in float32 (times ``std``), then
   each tensor is quantized on its own: descale = max|x| / 448 and the E4M3
   codes are ``(x / descale)`` rounded by PyTorch's float8_e4m3fn conversion
@@ -174,6 +176,12 @@ class Fp8PrefillCase:
         return 4.0 * self.B * self.H * self.D * visible_pairs(self.S_q, self.S_kv, self.causal)
 
 
+# Backward of the C2 forward shape (bf16, non-causal and causal).
+C8 = PrefillCase("prefill_bwd_bhsd_bf16_b4_h32_s4096_d128", 4, 32, 4096, 4096, 128, "bhsd", "bf16",
+                 False)
+C8_CAUSAL = PrefillCase("prefill_bwd_bhsd_bf16_b4_h32_s4096_d128_causal", 4, 32, 4096, 4096, 128,
+                        "bhsd", "bf16", True)
+
 # The BHSD prefill shape of C2 with E4M3 inputs (the pages' "FAv3 - FP8" item).
 C7 = Fp8PrefillCase("prefill_fp8e4m3_bhsd_b4_h32_s4096_d128", 4, 32, 4096, 4096, 128, "bhsd",
                     False)
@@ -201,6 +209,18 @@ def _randn(g, shape, std, dtype):
 
 def prefill_shape(B, H, S, D, layout):
     return (B, H, S, D) if layout == "bhsd" else (B, S, H, D)
+
+
+def make_prefill_bwd(case: PrefillCase):
+    """Return CPU tensors (q, k, v, dout) for a backward case (q, k, v exactly as
+    make_prefill draws them)."""
+    g = _gen(case.seed)
+    dt = _DTYPES[case.dtype]
+    q = _randn(g, prefill_shape(case.B, case.H, case.S_q, case.D, case.layout), case.std, dt)
+    k = _randn(g, prefill_shape(case.B, case.H, case.S_kv, case.D, case.layout), case.std, dt)
+    v = _randn(g, prefill_shape(case.B, case.H, case.S_kv, case.D, case.layout), case.std, dt)
+    do = _randn(g, prefill_shape(case.B, case.H, case.S_q, case.D, case.layout), case.std, dt)
+    return q, k, v, do
 
 
 def make_prefill(case: PrefillCase):
