@@ -43,7 +43,7 @@ _STATUS_NAMES = {
 }
 
 # Names the header exports (checked against include/attn_gb300.h by the tests).
-EXPORTED = ("attn_prefill_fwd", "attn_prefill_fp8_fwd", "attn_extend_fwd", "attn_decode_fwd", "attn_decode_fwd_noalloc",
+EXPORTED = ("attn_prefill_fwd", "attn_prefill_bwd", "attn_prefill_fp8_fwd", "attn_extend_fwd", "attn_decode_fwd", "attn_decode_fwd_noalloc",
             "attn_last_error",
             "attn_device_error", "attn_set_wait_limit_ns", "attn_release_workspace",
             "attn_version")
@@ -77,6 +77,8 @@ def lib() -> ctypes.CDLL:
             L.attn_prefill_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, cf,
                                            vp]
             L.attn_prefill_fwd.restype = ci
+            L.attn_prefill_bwd.argtypes = [vp] * 10 + [ci] * 8 + [cf, vp]
+            L.attn_prefill_bwd.restype = ci
             L.attn_prefill_fp8_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci,
                                                cf, cf, cf, cf, vp]
             L.attn_prefill_fp8_fwd.restype = ci
@@ -120,6 +122,13 @@ def attn_prefill_fwd(q, k, v, o, lse, B, H, S_q, S_kv, D, layout, dtype, causal,
     """C ``attn_prefill_fwd``; pointers and stream as ints.  Returns the status."""
     return lib().attn_prefill_fwd(q, k, v, o, lse, B, H, S_q, S_kv, D, layout, dtype, causal,
                                   scale, stream)
+
+
+def attn_prefill_bwd(q, k, v, o, dout, lse, dq, dk, dv, delta, B, H, S_q, S_kv, D, layout,
+                     dtype, causal, scale, stream) -> int:
+    """C ``attn_prefill_bwd``; pointers and stream as ints.  Returns the status."""
+    return lib().attn_prefill_bwd(q, k, v, o, dout, lse, dq, dk, dv, delta, B, H, S_q, S_kv, D,
+                                  layout, dtype, causal, scale, stream)
 
 
 def attn_prefill_fp8_fwd(q, k, v, o, lse, B, H, S_q, S_kv, D, layout, out_dtype, causal, scale,
@@ -245,6 +254,40 @@ def prefill(q, k, v, *, causal: bool = False, scale: float | None = None,
     return (out, lse) if return_lse else out
 
 
+def prefill_bwd(q, k, v, o, dout, lse, *, causal: bool = False, scale: float | None = None,
+                layout: str = "bhsd", dq=None, dk=None, dv=None, delta=None, stream=None):
+    """Gradients (dq, dk, dv) of ``o = prefill(q, k, v)`` for the upstream
+    gradient ``dout``, given the forward's ``o`` and ``lse``; torch CUDA tensors
+    in the forward's layout.  D must be 128.  ``dq``/``dk``/``dv`` and the fp32
+    [B,H,S_q] scratch ``delta`` may be passed in preallocated."""
+    torch = _torch()
+    _require_cuda(q, k, v, o, dout, lse)
+    if layout == "bhsd":
+        B, H, S_q, D = q.shape
+        S_kv = k.shape[2]
+        code = ATTN_BHSD
+    elif layout == "bshd":
+        B, S_q, H, D = q.shape
+        S_kv = k.shape[1]
+        code = ATTN_BSHD
+    else:
+        raise ValueError("layout must be 'bhsd' or 'bshd'")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if delta is None:
+        delta = torch.empty((B, H, S_q), device=q.device, dtype=torch.float32)
+    _require_cuda(dq, dk, dv, delta)
+    _check(attn_prefill_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                            dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                            dv.data_ptr(), delta.data_ptr(), B, H, S_q, S_kv, D, code,
+                            _dtype_code(q), int(bool(causal)), float(scale),
+                            _stream_handle(stream)))
+    return dq, dk, dv
+
+
 def prefill_fp8(q, k, v, *, descale_q: float, descale_k: float, descale_v: float,
                 causal: bool = False, scale: float | None = None, layout: str = "bhsd",
                 out_dtype=None, out=None, lse=None, return_lse: bool = False, stream=None):
@@ -365,4 +408,4 @@ def check_device_error() -> None:
 
 
 __all__ = [n for n in dir() if n.startswith(("attn_", "ATTN_"))] + [
-    "AttnError", "prefill", "prefill_fp8", "extend", "decode", "lib", "library_path", "check_device_error", "EXPORTED"]
+    "AttnError", "prefill", "prefill_bwd", "prefill_fp8", "extend", "decode", "lib", "library_path", "check_device_error", "EXPORTED"]

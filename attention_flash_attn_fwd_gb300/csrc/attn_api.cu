@@ -13,6 +13,7 @@
 #include <unordered_map>
 
 #include "../../include/attn_gb300.h"
+#include "backward_sm103a.h"
 #include "decode_sm103a.h"
 #include "prefill_sm103a.h"
 #include "tmap.h"
@@ -257,6 +258,72 @@ attn_status attn_prefill_fwd(const void* q, const void* k, const void* v, void* 
   p.wait_limit_ns = g_wait_limit_ns.load();
   cudaError_t e = attn_sm103a::prefill_launch(mq, mk, mv, mo, p, D, bf16, stream);
   if (e != cudaSuccess) return fail_cuda(e, "prefill launch");
+  return ATTN_OK;
+}
+
+attn_status attn_prefill_bwd(const void* q, const void* k, const void* v, const void* o,
+                             const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                             float* delta, int B, int H, int S_q, int S_kv, int D,
+                             attn_layout layout, attn_dtype dtype, int causal, float scale,
+                             cudaStream_t stream) {
+  if (B < 0 || H < 0 || S_q < 0 || S_kv < 0)
+    return fail(ATTN_ERR_INVALID_ARG, "B, H, S_q and S_kv must be >= 0");
+  if (layout != ATTN_BHSD && layout != ATTN_BSHD)
+    return fail(ATTN_ERR_INVALID_ARG, "layout must be ATTN_BHSD or ATTN_BSHD");
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16)
+    return fail(ATTN_ERR_INVALID_ARG, "dtype must be ATTN_F16 or ATTN_BF16");
+  if (causal != 0 && causal != 1) return fail(ATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (!(std::isfinite(scale) && scale > 0.f))
+    return fail(ATTN_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (D != 128) return fail(ATTN_ERR_UNSUPPORTED, "the backward supports D = 128 only");
+  if (static_cast<int64_t>(B) * H == 0 || (S_q == 0 && S_kv == 0)) return ATTN_OK;
+  if (S_q == 0 || S_kv == 0)
+    return fail(ATTN_ERR_UNSUPPORTED, "the backward needs S_q > 0 and S_kv > 0");
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !delta)
+    return fail(ATTN_ERR_INVALID_ARG, "every tensor pointer must be non-NULL");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return fail(ATTN_ERR_INVALID_ARG, "q, k, v, o, dout, dq, dk and dv must be 16-byte aligned");
+  const int64_t elems = static_cast<int64_t>(B) * H * (S_q > S_kv ? S_q : S_kv) * D;
+  if (elems * 2 >= (int64_t(1) << 40))
+    return fail(ATTN_ERR_UNSUPPORTED, "tensor too large for one TMA descriptor");
+  const int64_t tiles = static_cast<int64_t>(B) * H * ((S_q > S_kv ? S_q : S_kv) + 127) / 128;
+  if (tiles > 0x7FFFFFFF || static_cast<int64_t>(B) * H * S_q / 8 > 0x7FFFFFFF)
+    return fail(ATTN_ERR_UNSUPPORTED, "grid too large");
+
+  DeviceState* st = nullptr;
+  attn_status s = device_state(&st);
+  if (s != ATTN_OK) return s;
+
+  const bool bshd = layout == ATTN_BSHD;
+  const bool bf16 = dtype == ATTN_BF16;
+  CUtensorMap mq, mk, mv, mdo, mdq, mdk, mdv;
+  if (!prefill_map(&mq, q, B, H, S_q, D, bshd, bf16) ||
+      !prefill_map(&mk, k, B, H, S_kv, D, bshd, bf16) ||
+      !prefill_map(&mv, v, B, H, S_kv, D, bshd, bf16) ||
+      !prefill_map(&mdo, dout, B, H, S_q, D, bshd, bf16) ||
+      !prefill_map(&mdq, dq, B, H, S_q, D, bshd, bf16) ||
+      !prefill_map(&mdk, dk, B, H, S_kv, D, bshd, bf16) ||
+      !prefill_map(&mdv, dv, B, H, S_kv, D, bshd, bf16))
+    return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed for a backward tensor");
+
+  attn_sm103a::BackwardParams p{};
+  p.o = o;
+  p.dout = dout;
+  p.lse = lse;
+  p.delta = delta;
+  p.B = B;
+  p.H = H;
+  p.S_q = S_q;
+  p.S_kv = S_kv;
+  p.causal = causal;
+  p.bshd = bshd ? 1 : 0;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.err = st->err_word;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  cudaError_t e = attn_sm103a::backward_launch(mq, mk, mv, mdo, mdq, mdk, mdv, p, bf16, stream);
+  if (e != cudaSuccess) return fail_cuda(e, "backward launch");
   return ATTN_OK;
 }
 

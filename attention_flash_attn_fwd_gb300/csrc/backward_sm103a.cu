@@ -1,0 +1,577 @@
+// backward_sm103a.cu -- attention backward (dQ, dK, dV) for sm_103a, D = 128.
+//
+// The gradients of O = softmax(scale Q K^T + causal mask) V for an upstream
+// gradient dO ("Backward Flash Attention", Wave February 2025 Release,
+// EvoFormer list; "Functionality & Performance on backward attention",
+// Milestones).  With P recomputed from the forward's lse,
+//
+//     D_i   = dO_i . O_i                      (delta kernel)
+//     dS_ij = P_ij (dO_i . v_j - D_i)
+//     dV_j  = sum_i P_ij dO_i,  dK_j = scale sum_i dS_ij q_i   (dK/dV kernel)
+//     dQ_i  = scale sum_j dS_ij k_j                            (dQ kernel)
+//
+// Two tensor-core kernels, each with one 128-row tile per CTA:
+//  * dK/dV: a CTA owns 128 keys (K, V resident in shared memory) and walks the
+//    query tiles that see them.  Per tile: S^T = K Q^T and dP^T = V dO^T into
+//    tensor memory; one thread per key row turns them into P^T and dS^T in
+//    place (16-bit pairs over the first half of each); dV += P^T dO and
+//    dK += dS^T Q read P^T / dS^T straight from tensor memory.  Tensor memory:
+//    S^T [0,128), dP^T [128,256), dV [256,384), dK [384,512).
+//  * dQ: a CTA owns 128 queries (Q, dO resident) and walks the key tiles they
+//    see: S = Q K^T, dP = dO V^T, P and dS in place, dQ += dS K.  Tensor
+//    memory: S [0,128), dP [128,256) (dS in its first half), dQ [256,384).
+// The dQ pass recomputes S and dP (7 MMAs per tile pair instead of 5) so that
+// no tile's gradient needs atomic accumulation: results are deterministic.
+// A TMA warp streams the walking tiles through a 2-stage ring, an MMA warp
+// issues tcgen05.mma, four warps do the element-wise work; every wait is
+// bounded in time.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <type_traits>
+
+#include "backward_sm103a.h"
+#include "sm103a_ptx.cuh"
+
+namespace attn_sm103a {
+
+namespace {
+
+constexpr int kT = 128;                    // rows per tile (queries or keys), and D
+constexpr int kTile = kT * kT * 2;         // one 16-bit 128 x 128 tile (two 64-column panels)
+constexpr int kPanel = kT * 128;           // one 64-column panel: 128 rows x 128 bytes
+constexpr int kThreadsB = 192;             // 4 element-wise warps, TMA warp, MMA warp
+constexpr int kWarpLoad = 4;
+constexpr int kWarpMmaB = 5;
+constexpr int kRing = 2;                   // stages of the walking pair of tiles
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct BwdCtl {
+  uint64_t res_full;          // the resident pair of tiles has landed
+  uint64_t full[kRing];       // walking pair (+ its lse/delta rows) has landed
+  uint64_t empty[kRing];      // the MMAs reading a stage are done
+  uint64_t mm_full;           // the two products of a step are in tensor memory
+  uint64_t ew_done;           // the element-wise pass of a step is in tensor memory
+  uint64_t mma_done;          // every MMA of the CTA has completed
+  uint64_t tmem_free;         // the element-wise warps are done with tensor memory
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(BwdCtl) <= 256, "control block must fit its reserved bytes");
+
+// Shared memory: resident A (32 KB) | resident B (32 KB) | ring of kRing x
+// (two 32 KB tiles) | per stage 2 x 128 floats (lse*log2e, delta) | control.
+constexpr int kOffRing = 2 * kTile;
+constexpr int kOffRows = kOffRing + kRing * 2 * kTile;
+constexpr int kOffCtl = kOffRows + kRing * 2 * kT * 4;
+constexpr int kSmemB = kOffCtl + 256 + 1024;
+
+__device__ __forceinline__ void load_tile(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                          int row, int h, int b, int bshd) {
+  for (int x = 0; x < 2; ++x) {
+    void* d = static_cast<uint8_t*>(dst) + x * kPanel;
+    if (bshd)
+      tma_load_4d(d, map, bar, x * 64, h, row, b);
+    else
+      tma_load_4d(d, map, bar, x * 64, row, h, b);
+  }
+}
+
+__device__ __forceinline__ void store_tile(const CUtensorMap* map, const void* src, int row,
+                                           int h, int b, int bshd) {
+  for (int x = 0; x < 2; ++x) {
+    const void* s = static_cast<const uint8_t*>(src) + x * kPanel;
+    if (bshd)
+      tma_store_4d(map, s, x * 64, h, row, b);
+    else
+      tma_store_4d(map, s, x * 64, row, h, b);
+  }
+}
+
+// A . B^T over D = 128 into tensor memory: both operands K-major (128-byte
+// swizzle, 8-row groups 1024 B apart), M = N = 128, K = 16 per instruction.
+__device__ __forceinline__ void mma_abt(uint32_t d, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
+                                        uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < kT / 16; ++kk) {
+    const uint32_t off = ((kk / 4) * kPanel + (kk % 4) * 32) >> 4;
+    mma_ss_lh(d, a_lo + off, hi, b_lo + off, hi, idesc, kk > 0);
+  }
+}
+
+// D (+)= A . B with A = 128 x 128 16-bit pairs in tensor memory (columns
+// [a, a + 64)) and B = a 128-row tile read MN-major (rows are the K index).
+__device__ __forceinline__ void mma_tmem_a(uint32_t d, uint32_t a, uint32_t b_lo, uint32_t hi,
+                                           uint32_t idesc, bool acc) {
+#pragma unroll
+  for (int kk = 0; kk < kT / 16; ++kk)
+    mma_ts_lh(d, a + kk * 8, b_lo + ((kk * 16 * 128) >> 4), hi, idesc,
+              (acc || kk > 0) ? 1u : 0u);
+}
+
+// Row-major 16-bit O/dO row r of 128 columns into 128-byte-swizzled staging
+// (two 64-column panels), from 64 fp32 values per call (columns [64h, 64h+64)).
+template <bool kBF16>
+__device__ __forceinline__ void stage_row(uint8_t* tile, int r, int h, const uint32_t (&v)[64],
+                                          float mul) {
+  uint8_t* sub = tile + h * kPanel + r * 128;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    uint4 w;
+    uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      wp[e] = pack2<kBF16>(__uint_as_float(v[q * 8 + 2 * e]) * mul,
+                           __uint_as_float(v[q * 8 + 2 * e + 1]) * mul);
+    *reinterpret_cast<uint4*>(sub + ((q ^ (r & 7)) * 16)) = w;
+  }
+}
+
+// Element-wise pass over one 128 x 128 step, in place in tensor memory:
+// S (fp32, columns [cs, cs+128)) -> P (16-bit pairs, [cs, cs+64)),
+// dP (fp32, [cd, cd+128)) -> dS = P (dP - delta) (16-bit pairs, [cd, cd+64)).
+// `lse2_of(c)` / `delta_of(c)` give the row statistics for column c (dK/dV
+// kernel: per query column) or are constant (dQ kernel: per thread's row);
+// `visible(c)` masks causal and ragged positions.
+template <bool kBF16, class Lse, class Delta, class Vis>
+__device__ __forceinline__ void elementwise_step(uint32_t lane_addr, uint32_t cs, uint32_t cd,
+                                                 float c, Lse lse2_of, Delta delta_of,
+                                                 Vis visible) {
+#pragma unroll 1
+  for (int ch = 0; ch < 4; ++ch) {  // 32 columns per chunk
+    uint32_t x[32], y[32];
+    tmem_ld32_wait(lane_addr + cs + ch * 32, x);
+    tmem_ld32_wait(lane_addr + cd + ch * 32, y);
+    uint32_t pp[16], dd[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      float pv[2], dv[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int col = ch * 32 + 2 * q + e;
+        const float arg = __uint_as_float(x[2 * q + e]) * c - lse2_of(col);
+        const float pe = visible(col) ? ex2_approx(arg) : 0.f;
+        pv[e] = pe;
+        dv[e] = pe * (__uint_as_float(y[2 * q + e]) - delta_of(col));
+      }
+      pp[q] = pack2<kBF16>(pv[0], pv[1]);
+      dd[q] = pack2<kBF16>(dv[0], dv[1]);
+    }
+    // Columns [16ch, 16ch + 16) were read by this chunk or an earlier one.
+    tmem_st16(lane_addr + cs + ch * 16, pp);
+    tmem_st16(lane_addr + cd + ch * 16, dd);
+  }
+  tmem_st_wait();
+}
+
+// ---------------------------------------------------------------- delta
+
+// delta[b,h,i] = sum_d dO[b,h,i,d] * O[b,h,i,d] in fp32; one warp per row.
+template <bool kBF16>
+__global__ void __launch_bounds__(256) bwd_delta_kernel(const BackwardParams p) {
+  using T = typename std::conditional<kBF16, __nv_bfloat16, __half>::type;
+  const long long rows = static_cast<long long>(p.B) * p.H * p.S_q;
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  if (row >= rows) return;
+  const int i = static_cast<int>(row % p.S_q);
+  const int bh = static_cast<int>(row / p.S_q);
+  const int b = bh / p.H, h = bh % p.H;
+  const size_t off = p.bshd ? ((static_cast<size_t>(b) * p.S_q + i) * p.H + h) * kT
+                            : ((static_cast<size_t>(b) * p.H + h) * p.S_q + i) * kT;
+  const uint2 a = *reinterpret_cast<const uint2*>(static_cast<const T*>(p.o) + off + lane * 4);
+  const uint2 g = *reinterpret_cast<const uint2*>(static_cast<const T*>(p.dout) + off + lane * 4);
+  const T* av = reinterpret_cast<const T*>(&a);
+  const T* gv = reinterpret_cast<const T*>(&g);
+  float s = 0.f;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) s += static_cast<float>(av[e]) * static_cast<float>(gv[e]);
+#pragma unroll
+  for (int m = 16; m > 0; m >>= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
+  if (lane == 0) p.delta[row] = s;
+}
+
+// ---------------------------------------------------------------- dK / dV
+
+template <bool kBF16>
+__global__ void __launch_bounds__(kThreadsB, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_do,
+                    const __grid_constant__ CUtensorMap tm_dk,
+                    const __grid_constant__ CUtensorMap tm_dv, const BackwardParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* s_k = smem;
+  uint8_t* s_v = smem + kTile;
+  float* s_rows = reinterpret_cast<float*>(smem + kOffRows);  // [stage][lse2 | delta][128]
+  BwdCtl* ctl = reinterpret_cast<BwdCtl*>(smem + kOffCtl);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  const int nkt = (p.S_kv + kT - 1) / kT;
+  const int bh = blockIdx.x / nkt;
+  const int kt = blockIdx.x % nkt;
+  const int b = bh / p.H, h = bh % p.H;
+  const int key0 = kt * kT;
+  const int off = p.S_kv - p.S_q;  // bottom-right causal offset
+  const int nqt = (p.S_q + kT - 1) / kT;
+  // Query tiles that see any key of this tile: rows i >= key0 - off (causal).
+  int first = 0;
+  if (p.causal) first = max(0, key0 - off) / kT;
+  const int n_steps = (p.causal && key0 - off > p.S_q - 1) ? 0 : nqt - first;
+
+  if (warp == kWarpMmaB) {
+    tmem_alloc(&ctl->tmem_base, 512);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(&ctl->res_full, 1);
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(&ctl->full[s], 2);  // TMA bytes + the row statistics
+      mbar_init(&ctl->empty[s], 1);
+    }
+    mbar_init(&ctl->mm_full, 1);
+    mbar_init(&ctl->ew_done, 4);
+    mbar_init(&ctl->mma_done, 1);
+    mbar_init(&ctl->tmem_free, 4);
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = ctl->tmem_base;
+  volatile int* abort_flag = &ctl->abort;
+
+  if (warp == kWarpLoad) {
+    // ---------------------------------------------------------- producer
+    if (n_steps > 0) {
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&ctl->res_full, 2 * kTile);
+        load_tile(s_k, &tm_k, &ctl->res_full, key0, h, b, p.bshd);
+        load_tile(s_v, &tm_v, &ctl->res_full, key0, h, b, p.bshd);
+      }
+      int issued = 0;
+      for (int s = 0; s < n_steps; ++s) {
+        if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+        const int st = s % kRing;
+        bool ok = true;
+        if (lane == 0 && s >= kRing)
+          ok = mbar_wait(&ctl->empty[st], (s / kRing - 1) & 1, p.wait_limit_ns, p.err, 60);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
+          if (lane == 0) *abort_flag = 1;
+          break;
+        }
+        const int q0 = (first + s) * kT;
+        uint8_t* stage = smem + kOffRing + st * 2 * kTile;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&ctl->full[st], 2 * kTile);
+          load_tile(stage, &tm_q, &ctl->full[st], q0, h, b, p.bshd);
+          load_tile(stage + kTile, &tm_do, &ctl->full[st], q0, h, b, p.bshd);
+        }
+        float* rows = s_rows + st * 2 * kT;
+        const size_t base = static_cast<size_t>(bh) * p.S_q;
+        for (int r = lane; r < kT; r += 32) {
+          const int i = q0 + r;
+          rows[r] = i < p.S_q ? p.lse[base + i] * kLog2e : 0.f;
+          rows[kT + r] = i < p.S_q ? p.delta[base + i] : 0.f;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->full[st]);
+        issued = s + 1;
+      }
+      if (lane == 0) {  // no copy may still be landing when the CTA exits
+        for (int s = max(0, issued - kRing); s < issued; ++s)
+          mbar_wait(&ctl->full[s % kRing], (s / kRing) & 1, p.wait_limit_ns, p.err, 61);
+        mbar_wait(&ctl->res_full, 0, p.wait_limit_ns, p.err, 62);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kWarpMmaB) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0 && n_steps > 0) {
+      constexpr uint32_t id_s = idesc_f16(kBF16, kT, kT, false, false);
+      constexpr uint32_t id_o = idesc_f16(kBF16, kT, kT, false, true);
+      const uint32_t hi = sdesc_hi_sw128(1024);
+      const uint32_t k_lo = sdesc_lo(smem_u32(s_k), 16);
+      const uint32_t v_lo = sdesc_lo(smem_u32(s_v), 16);
+      bool ok = mbar_wait(&ctl->res_full, 0, p.wait_limit_ns, p.err, 63);
+      for (int s = 0; s < n_steps && ok; ++s) {
+        const int st = s % kRing;
+        const uint32_t stage = smem_u32(smem + kOffRing + st * 2 * kTile);
+        if (!(ok = mbar_wait(&ctl->full[st], (s / kRing) & 1, p.wait_limit_ns, p.err, 64))) break;
+        tc_fence_after_sync();
+        mma_abt(tmem + 0, k_lo, sdesc_lo(stage, 16), hi, id_s);            // S^T = K Q^T
+        mma_abt(tmem + 128, v_lo, sdesc_lo(stage + kTile, 16), hi, id_s);  // dP^T = V dO^T
+        mma_commit(&ctl->mm_full);
+        if (!(ok = mbar_wait(&ctl->ew_done, s & 1, p.wait_limit_ns, p.err, 65))) break;
+        tc_fence_after_sync();
+        // dV += P^T dO and dK += dS^T Q, the walking tiles read MN-major
+        mma_tmem_a(tmem + 256, tmem + 0, sdesc_lo(stage + kTile, kPanel), hi, id_o, s > 0);
+        mma_tmem_a(tmem + 384, tmem + 128, sdesc_lo(stage, kPanel), hi, id_o, s > 0);
+        mma_commit(&ctl->empty[st]);
+      }
+      if (!ok) *abort_flag = 1;
+      mma_commit(&ctl->mma_done);
+      mbar_wait(&ctl->mma_done, 0, p.wait_limit_ns, p.err, 66);
+    }
+    __syncwarp();
+    mbar_wait(&ctl->tmem_free, 0, p.wait_limit_ns, p.err, 67);
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  } else {
+    // ---------------------------------------------------------- element-wise
+    const int r = warp * 32 + lane;   // key row within the tile
+    const int key = key0 + r;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    bool ok = true;
+    for (int s = 0; s < n_steps; ++s) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&ctl->mm_full, s & 1, p.wait_limit_ns, p.err, 70));
+      if (!ok) break;
+      tc_fence_after_sync();
+      const int st = s % kRing;
+      const float* lse2 = s_rows + st * 2 * kT;
+      const float* dlt = lse2 + kT;
+      const int q0 = (first + s) * kT;
+      const bool full = key0 + kT <= p.S_kv && q0 + kT <= p.S_q &&
+                        (!p.causal || key0 + kT - 1 <= q0 + off);
+      elementwise_step<kBF16>(
+          lane_addr, 0, 128, p.scale_log2, [&](int col) { return lse2[col]; },
+          [&](int col) { return dlt[col]; },
+          [&](int col) {
+            const int i = q0 + col;
+            return full || (key < p.S_kv && i < p.S_q && (!p.causal || key <= i + off));
+          });
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->ew_done);
+    }
+    // ---------------------------------------------------------- epilogue
+    if (ok && n_steps > 0)
+      ok = __all_sync(0xffffffffu, mbar_wait(&ctl->mma_done, 0, p.wait_limit_ns, p.err, 71));
+    tc_fence_after_sync();
+    const bool have = ok && n_steps > 0;
+    // dV into the V tile, dK (times scale) into the K tile: both are dead.
+#pragma unroll 1
+    for (int hh = 0; hh < 2; ++hh) {
+      uint32_t o[64] = {};
+      if (have) tmem_ld64_wait(lane_addr + 256 + hh * 64, o);
+      stage_row<kBF16>(s_v, r, hh, o, 1.f);
+      if (have) tmem_ld64_wait(lane_addr + 384 + hh * 64, o);
+      stage_row<kBF16>(s_k, r, hh, o, p.scale);
+    }
+    tc_fence_before_sync();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl->tmem_free);
+    fence_proxy_async_smem();
+    named_barrier_sync(1, 128);
+    if (threadIdx.x == 0) {
+      store_tile(&tm_dv, s_v, key0, h, b, p.bshd);
+      store_tile(&tm_dk, s_k, key0, h, b, p.bshd);
+      tma_store_commit();
+      tma_store_wait_all();
+    }
+    __syncwarp();
+  }
+}
+
+// ---------------------------------------------------------------- dQ
+
+template <bool kBF16>
+__global__ void __launch_bounds__(kThreadsB, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
+                  const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v,
+                  const __grid_constant__ CUtensorMap tm_do,
+                  const __grid_constant__ CUtensorMap tm_dq, const BackwardParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* s_q = smem;
+  uint8_t* s_do = smem + kTile;
+  BwdCtl* ctl = reinterpret_cast<BwdCtl*>(smem + kOffCtl);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  const int nqt = (p.S_q + kT - 1) / kT;
+  const int bh = blockIdx.x / nqt;
+  const int qt = blockIdx.x % nqt;
+  const int b = bh / p.H, h = bh % p.H;
+  const int q0 = qt * kT;
+  const int off = p.S_kv - p.S_q;
+  int keys = p.S_kv;
+  if (p.causal) keys = min(keys, min(q0 + kT, p.S_q) - 1 + off + 1);
+  const int n_steps = keys <= 0 ? 0 : (keys + kT - 1) / kT;
+
+  if (warp == kWarpMmaB) {
+    tmem_alloc(&ctl->tmem_base, 512);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(&ctl->res_full, 1);
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(&ctl->full[s], 1);
+      mbar_init(&ctl->empty[s], 1);
+    }
+    mbar_init(&ctl->mm_full, 1);
+    mbar_init(&ctl->ew_done, 4);
+    mbar_init(&ctl->mma_done, 1);
+    mbar_init(&ctl->tmem_free, 4);
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = ctl->tmem_base;
+  volatile int* abort_flag = &ctl->abort;
+
+  if (warp == kWarpLoad) {
+    if (lane == 0 && n_steps > 0) {
+      mbar_arrive_expect_tx(&ctl->res_full, 2 * kTile);
+      load_tile(s_q, &tm_q, &ctl->res_full, q0, h, b, p.bshd);
+      load_tile(s_do, &tm_do, &ctl->res_full, q0, h, b, p.bshd);
+      int issued = 0;
+      for (int s = 0; s < n_steps && !*abort_flag; ++s) {
+        const int st = s % kRing;
+        if (s >= kRing &&
+            !mbar_wait(&ctl->empty[st], (s / kRing - 1) & 1, p.wait_limit_ns, p.err, 80)) {
+          *abort_flag = 1;
+          break;
+        }
+        uint8_t* stage = smem + kOffRing + st * 2 * kTile;
+        mbar_arrive_expect_tx(&ctl->full[st], 2 * kTile);
+        load_tile(stage, &tm_k, &ctl->full[st], s * kT, h, b, p.bshd);
+        load_tile(stage + kTile, &tm_v, &ctl->full[st], s * kT, h, b, p.bshd);
+        issued = s + 1;
+      }
+      for (int s = max(0, issued - kRing); s < issued; ++s)
+        mbar_wait(&ctl->full[s % kRing], (s / kRing) & 1, p.wait_limit_ns, p.err, 81);
+      mbar_wait(&ctl->res_full, 0, p.wait_limit_ns, p.err, 82);
+    }
+    __syncwarp();
+  } else if (warp == kWarpMmaB) {
+    if (lane == 0 && n_steps > 0) {
+      constexpr uint32_t id_s = idesc_f16(kBF16, kT, kT, false, false);
+      constexpr uint32_t id_o = idesc_f16(kBF16, kT, kT, false, true);
+      const uint32_t hi = sdesc_hi_sw128(1024);
+      const uint32_t q_lo = sdesc_lo(smem_u32(s_q), 16);
+      const uint32_t do_lo = sdesc_lo(smem_u32(s_do), 16);
+      bool ok = mbar_wait(&ctl->res_full, 0, p.wait_limit_ns, p.err, 83);
+      for (int s = 0; s < n_steps && ok; ++s) {
+        const int st = s % kRing;
+        const uint32_t stage = smem_u32(smem + kOffRing + st * 2 * kTile);
+        if (!(ok = mbar_wait(&ctl->full[st], (s / kRing) & 1, p.wait_limit_ns, p.err, 84))) break;
+        tc_fence_after_sync();
+        mma_abt(tmem + 0, q_lo, sdesc_lo(stage, 16), hi, id_s);            // S = Q K^T
+        mma_abt(tmem + 128, do_lo, sdesc_lo(stage + kTile, 16), hi, id_s);  // dP = dO V^T
+        mma_commit(&ctl->mm_full);
+        if (!(ok = mbar_wait(&ctl->ew_done, s & 1, p.wait_limit_ns, p.err, 85))) break;
+        tc_fence_after_sync();
+        // dQ += dS K (dS in columns [128, 192)), K read MN-major
+        mma_tmem_a(tmem + 256, tmem + 128, sdesc_lo(stage, kPanel), hi, id_o, s > 0);
+        mma_commit(&ctl->empty[st]);
+      }
+      if (!ok) *abort_flag = 1;
+      mma_commit(&ctl->mma_done);
+      mbar_wait(&ctl->mma_done, 0, p.wait_limit_ns, p.err, 86);
+    }
+    __syncwarp();
+    mbar_wait(&ctl->tmem_free, 0, p.wait_limit_ns, p.err, 87);
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  } else {
+    const int r = warp * 32 + lane;  // query row within the tile
+    const int i = q0 + r;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const size_t ridx = static_cast<size_t>(bh) * p.S_q + i;
+    const float lse2 = i < p.S_q ? p.lse[ridx] * kLog2e : 0.f;
+    const float dlt = i < p.S_q ? p.delta[ridx] : 0.f;
+    bool ok = true;
+    for (int s = 0; s < n_steps; ++s) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&ctl->mm_full, s & 1, p.wait_limit_ns, p.err, 90));
+      if (!ok) break;
+      tc_fence_after_sync();
+      const int k0 = s * kT;
+      const bool full = k0 + kT <= p.S_kv && q0 + kT <= p.S_q &&
+                        (!p.causal || k0 + kT - 1 <= q0 + off);
+      elementwise_step<kBF16>(
+          lane_addr, 0, 128, p.scale_log2, [&](int) { return lse2; }, [&](int) { return dlt; },
+          [&](int col) {
+            const int key = k0 + col;
+            return full || (key < p.S_kv && i < p.S_q && (!p.causal || key <= i + off));
+          });
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->ew_done);
+    }
+    if (ok && n_steps > 0)
+      ok = __all_sync(0xffffffffu, mbar_wait(&ctl->mma_done, 0, p.wait_limit_ns, p.err, 91));
+    tc_fence_after_sync();
+    const bool have = ok && n_steps > 0;
+#pragma unroll 1
+    for (int hh = 0; hh < 2; ++hh) {  // dQ (times scale) into the Q tile, dead now
+      uint32_t o[64] = {};
+      if (have) tmem_ld64_wait(lane_addr + 256 + hh * 64, o);
+      stage_row<kBF16>(s_q, r, hh, o, p.scale);
+    }
+    tc_fence_before_sync();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl->tmem_free);
+    fence_proxy_async_smem();
+    named_barrier_sync(1, 128);
+    if (threadIdx.x == 0) {
+      store_tile(&tm_dq, s_q, q0, h, b, p.bshd);
+      tma_store_commit();
+      tma_store_wait_all();
+    }
+    __syncwarp();
+  }
+}
+
+template <class K>
+cudaError_t configure(K kern) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemB);
+}
+
+template <bool kBF16>
+cudaError_t launch_all(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                       const CUtensorMap& dout, const CUtensorMap& dq, const CUtensorMap& dk,
+                       const CUtensorMap& dv, const BackwardParams& p, cudaStream_t stream) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = configure(bwd_dkdv_kernel<kBF16>);
+    if (e == cudaSuccess) e = configure(bwd_dq_kernel<kBF16>);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const long long rows = static_cast<long long>(p.B) * p.H * p.S_q;
+  if (rows > 0) {
+    bwd_delta_kernel<kBF16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  const int nkt = (p.S_kv + kT - 1) / kT;
+  const int nqt = (p.S_q + kT - 1) / kT;
+  if (p.B * p.H * nkt > 0)
+    bwd_dkdv_kernel<kBF16><<<p.B * p.H * nkt, kThreadsB, kSmemB, stream>>>(q, k, v, dout, dk,
+                                                                           dv, p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (p.B * p.H * nqt > 0)
+    bwd_dq_kernel<kBF16><<<p.B * p.H * nqt, kThreadsB, kSmemB, stream>>>(q, k, v, dout, dq, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t backward_launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                            const CUtensorMap& dout, const CUtensorMap& dq, const CUtensorMap& dk,
+                            const CUtensorMap& dv, const BackwardParams& p, bool bf16,
+                            cudaStream_t stream) {
+  return bf16 ? launch_all<true>(q, k, v, dout, dq, dk, dv, p, stream)
+              : launch_all<false>(q, k, v, dout, dq, dk, dv, p, stream);
+}
+
+}  // namespace attn_sm103a

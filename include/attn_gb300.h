@@ -83,6 +83,31 @@ ATTN_API attn_status attn_prefill_fwd(const void* q, const void* k, const void* 
                              attn_dtype dtype, int causal, float scale, cudaStream_t stream);
 
 /*
+ * Attention backward: gradients of attn_prefill_fwd's O.
+ *
+ * Defines, for the upstream gradient dO of O and P the softmax of the
+ * forward ("Backward Flash Attention", Wave February 2025 Release, EvoFormer
+ * list):  D_i = dO_i . O_i,  dS_ij = P_ij (dO_i . v_j - D_i),
+ *         dQ_i = scale sum_j dS_ij k_j,  dK_j = scale sum_i dS_ij q_i,
+ *         dV_j = sum_i P_ij dO_i  over the visible (i, j) pairs.
+ *
+ *   q, k, v, o  the forward's inputs and output (layout and dtype as there)
+ *   dout        dO, q's shape, layout and dtype
+ *   lse         [B,H,S_q] fp32, the lse the forward returned
+ *   dq, dk, dv  outputs, the shapes of q, k, v, same layout and dtype
+ *   delta       [B,H,S_q] fp32 scratch owned by the caller (overwritten with D)
+ *   D           128 only (else ATTN_ERR_UNSUPPORTED); S_q, S_kv > 0; other
+ *               arguments as for attn_prefill_fwd.
+ * Deterministic: no atomics; P and dS are rounded to the input dtype before
+ * their products, accumulation is fp32.  Allocates nothing.
+ */
+ATTN_API attn_status attn_prefill_bwd(const void* q, const void* k, const void* v, const void* o,
+                                      const void* dout, const float* lse, void* dq, void* dk,
+                                      void* dv, float* delta, int B, int H, int S_q, int S_kv,
+                                      int D, attn_layout layout, attn_dtype dtype, int causal,
+                                      float scale, cudaStream_t stream);
+
+/*
  * FP8 prefill attention forward: the prefill operation on E4M3 inputs.
  *
  * Defines: attn_prefill_fwd's O and lse for Q = descale_q * q, K = descale_k *

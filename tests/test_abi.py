@@ -111,6 +111,35 @@ def test_decode_empty_batch_is_a_no_op():
     assert _decode(B=0, num_pages=0) == attn.ATTN_OK
 
 
+def _bwd(**kw):
+    a = dict(q=16, k=16, v=16, o=16, dout=16, lse=16, dq=16, dk=16, dv=16, delta=16, B=1, H=1,
+             S_q=8, S_kv=8, D=128, layout=0, dtype=1, causal=0, scale=0.1, stream=None)
+    a.update(kw)
+    return attn.attn_prefill_bwd(**a)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(D=64), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(S_kv=0), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(layout=7), attn.ATTN_ERR_INVALID_ARG),
+    (dict(dtype=2), attn.ATTN_ERR_INVALID_ARG),
+    (dict(causal=5), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=-1.0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(B=-1), attn.ATTN_ERR_INVALID_ARG),
+    (dict(delta=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(lse=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(dk=8), attn.ATTN_ERR_INVALID_ARG),  # misaligned
+])
+def test_backward_rejects_bad_arguments(kw, code):
+    assert _bwd(**kw) == code
+    assert attn.attn_last_error()
+
+
+def test_backward_empty_problem_is_a_no_op():
+    assert _bwd(B=0, q=None) == attn.ATTN_OK
+    assert _bwd(S_q=0, S_kv=0) == attn.ATTN_OK
+
+
 def _prefill_fp8(**kw):
     a = dict(q=16, k=16, v=16, o=16, lse=None, B=1, H=1, S_q=8, S_kv=8, D=128, layout=0,
              out_dtype=1, causal=0, scale=0.1, descale_q=1.0, descale_k=1.0, descale_v=1.0,
