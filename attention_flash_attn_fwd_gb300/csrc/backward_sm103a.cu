@@ -23,8 +23,9 @@
 // The dQ pass recomputes S and dP (7 MMAs per tile pair instead of 5) so that
 // no tile's gradient needs atomic accumulation: results are deterministic.
 // A TMA warp streams the walking tiles through a 2-stage ring, an MMA warp
-// issues tcgen05.mma, four warps do the element-wise work; every wait is
-// bounded in time.
+// issues tcgen05.mma, eight warps do the element-wise work (two warpgroups,
+// each taking 64 of the 128 columns of every row); every wait is bounded in
+// time.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -40,9 +41,18 @@ namespace {
 constexpr int kT = 128;                    // rows per tile (queries or keys), and D
 constexpr int kTile = kT * kT * 2;         // one 16-bit 128 x 128 tile (two 64-column panels)
 constexpr int kPanel = kT * 128;           // one 64-column panel: 128 rows x 128 bytes
-constexpr int kThreadsB = 192;             // 4 element-wise warps, TMA warp, MMA warp
-constexpr int kWarpLoad = 4;
-constexpr int kWarpMmaB = 5;
+constexpr int kThreadsB = 384;  // 8 element-wise warps | TMA warp, MMA warp, 2 idle warps
+constexpr int kEwWarps = 8;
+constexpr int kWarpLoad = 8;
+constexpr int kWarpMmaB = 9;
+// Registers are granted per warpgroup: the block launches with 168 per
+// thread (64512 in all) and setmaxnreg gives the two element-wise warpgroups
+// 224, the control warpgroup 56 (2*128*224 + 128*56 = 64512).
+constexpr int kRegsLaunchB = 168;
+constexpr int kRegsEw = 224;
+constexpr int kRegsCtl = 56;
+static_assert(2 * 128 * kRegsEw + 128 * kRegsCtl <= kThreadsB * kRegsLaunchB,
+              "register split exceeds the block's launch allocation");
 constexpr int kRing = 2;                   // stages of the walking pair of tiles
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -127,39 +137,61 @@ __device__ __forceinline__ void stage_row(uint8_t* tile, int r, int h, const uin
   }
 }
 
-// Element-wise pass over one 128 x 128 step, in place in tensor memory:
+// Element-wise pass over one 128 x 128 step, in place in tensor memory.  The
+// calling warp owns column group g (columns [64g, 64g + 64)) of its 32 rows:
 // S (fp32, columns [cs, cs+128)) -> P (16-bit pairs, [cs, cs+64)),
 // dP (fp32, [cd, cd+128)) -> dS = P (dP - delta) (16-bit pairs, [cd, cd+64)).
-// `lse2_of(c)` / `delta_of(c)` give the row statistics for column c (dK/dV
-// kernel: per query column) or are constant (dQ kernel: per thread's row);
-// `visible(c)` masks causal and ragged positions.
-template <bool kBF16, class Lse, class Delta, class Vis>
-__device__ __forceinline__ void elementwise_step(uint32_t lane_addr, uint32_t cs, uint32_t cd,
-                                                 float c, Lse lse2_of, Delta delta_of,
-                                                 Vis visible) {
-#pragma unroll 1
-  for (int ch = 0; ch < 4; ++ch) {  // 32 columns per chunk
-    uint32_t x[32], y[32];
-    tmem_ld32_wait(lane_addr + cs + ch * 32, x);
-    tmem_ld32_wait(lane_addr + cd + ch * 32, y);
-    uint32_t pp[16], dd[16];
+// Packed pairs of group 1 land on fp32 columns of group 0, so every
+// element-wise warp loads its columns before any of them stores (barrier
+// `bar_id` over all element-wise threads).  `lse2_of(c)` / `delta_of(c)` give
+// the row statistics for column c (dK/dV kernel: per query column; dQ kernel:
+// constant per row); `visible(c)` masks causal and ragged positions and is
+// only evaluated when `masked`.
+template <bool kBF16, bool kMasked, int kHalf, class Lse, class Delta, class Vis>
+__device__ __forceinline__ void ew_compute(const uint32_t (&x)[64], const uint32_t (&y)[64],
+                                           uint32_t (&pp)[16], uint32_t (&dd)[16], int g,
+                                           float c, Lse lse2_of, Delta delta_of, Vis visible) {
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      float pv[2], dv[2];
+  for (int q = 16 * kHalf; q < 16 * kHalf + 16; ++q) {
+    float pv[2], dv[2];
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int col = ch * 32 + 2 * q + e;
-        const float arg = __uint_as_float(x[2 * q + e]) * c - lse2_of(col);
-        const float pe = visible(col) ? ex2_approx(arg) : 0.f;
-        pv[e] = pe;
-        dv[e] = pe * (__uint_as_float(y[2 * q + e]) - delta_of(col));
-      }
-      pp[q] = pack2<kBF16>(pv[0], pv[1]);
-      dd[q] = pack2<kBF16>(dv[0], dv[1]);
+    for (int e = 0; e < 2; ++e) {
+      const int col = 64 * g + 2 * q + e;
+      float pe = ex2_approx(__uint_as_float(x[2 * q + e]) * c - lse2_of(col));
+      if constexpr (kMasked) pe = visible(col) ? pe : 0.f;
+      pv[e] = pe;
+      dv[e] = pe * (__uint_as_float(y[2 * q + e]) - delta_of(col));
     }
-    // Columns [16ch, 16ch + 16) were read by this chunk or an earlier one.
-    tmem_st16(lane_addr + cs + ch * 16, pp);
-    tmem_st16(lane_addr + cd + ch * 16, dd);
+    pp[q - 16 * kHalf] = pack2<kBF16>(pv[0], pv[1]);
+    dd[q - 16 * kHalf] = pack2<kBF16>(dv[0], dv[1]);
+  }
+}
+
+template <bool kBF16, class Lse, class Delta, class Vis>
+__device__ __forceinline__ void elementwise_step(uint32_t lane_addr, int g, uint32_t cs,
+                                                 uint32_t cd, float c, bool masked, int bar_id,
+                                                 Lse lse2_of, Delta delta_of, Vis visible) {
+  uint32_t x[64], y[64];
+  tmem_ld64_wait(lane_addr + cs + 64 * g, x);
+  tmem_ld64_wait(lane_addr + cd + 64 * g, y);
+  named_barrier_sync(bar_id, kEwWarps * 32);
+  {
+    uint32_t pp[16], dd[16];
+    if (masked)
+      ew_compute<kBF16, true, 0>(x, y, pp, dd, g, c, lse2_of, delta_of, visible);
+    else
+      ew_compute<kBF16, false, 0>(x, y, pp, dd, g, c, lse2_of, delta_of, visible);
+    tmem_st16(lane_addr + cs + 32 * g, pp);
+    tmem_st16(lane_addr + cd + 32 * g, dd);
+  }
+  {
+    uint32_t pp[16], dd[16];
+    if (masked)
+      ew_compute<kBF16, true, 1>(x, y, pp, dd, g, c, lse2_of, delta_of, visible);
+    else
+      ew_compute<kBF16, false, 1>(x, y, pp, dd, g, c, lse2_of, delta_of, visible);
+    tmem_st16(lane_addr + cs + 32 * g + 16, pp);
+    tmem_st16(lane_addr + cd + 32 * g + 16, dd);
   }
   tmem_st_wait();
 }
@@ -233,9 +265,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       mbar_init(&ctl->empty[s], 1);
     }
     mbar_init(&ctl->mm_full, 1);
-    mbar_init(&ctl->ew_done, 4);
+    mbar_init(&ctl->ew_done, kEwWarps);
     mbar_init(&ctl->mma_done, 1);
-    mbar_init(&ctl->tmem_free, 4);
+    mbar_init(&ctl->tmem_free, kEwWarps);
     ctl->abort = 0;
     fence_mbar_init();
   }
@@ -245,7 +277,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   const uint32_t tmem = ctl->tmem_base;
   volatile int* abort_flag = &ctl->abort;
 
-  if (warp == kWarpLoad) {
+  if (warp >= kEwWarps) {
+   setmaxnreg_dec<kRegsCtl>();
+   if (warp == kWarpLoad) {
     // ---------------------------------------------------------- producer
     if (n_steps > 0) {
       if (lane == 0) {
@@ -289,7 +323,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       }
     }
     __syncwarp();
-  } else if (warp == kWarpMmaB) {
+   } else if (warp == kWarpMmaB) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0 && n_steps > 0) {
       constexpr uint32_t id_s = idesc_f16(kBF16, kT, kT, false, false);
@@ -321,11 +355,14 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     mbar_wait(&ctl->tmem_free, 0, p.wait_limit_ns, p.err, 67);
     tc_fence_after_sync();
     tmem_dealloc(tmem, 512);
+   }
   } else {
+    setmaxnreg_inc<kRegsEw>();
     // ---------------------------------------------------------- element-wise
-    const int r = warp * 32 + lane;   // key row within the tile
+    const int g = warp / 4;                // column group of this warp
+    const int r = (warp % 4) * 32 + lane;  // key row within the tile
     const int key = key0 + r;
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
     bool ok = true;
     for (int s = 0; s < n_steps; ++s) {
       ok = __all_sync(0xffffffffu, mbar_wait(&ctl->mm_full, s & 1, p.wait_limit_ns, p.err, 70));
@@ -338,11 +375,11 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       const bool full = key0 + kT <= p.S_kv && q0 + kT <= p.S_q &&
                         (!p.causal || key0 + kT - 1 <= q0 + off);
       elementwise_step<kBF16>(
-          lane_addr, 0, 128, p.scale_log2, [&](int col) { return lse2[col]; },
-          [&](int col) { return dlt[col]; },
-          [&](int col) {
+          lane_addr, g, 0, 128, p.scale_log2, !full, 2, [=](int col) { return lse2[col]; },
+          [=](int col) { return dlt[col]; },
+          [=](int col) {
             const int i = q0 + col;
-            return full || (key < p.S_kv && i < p.S_q && (!p.causal || key <= i + off));
+            return key < p.S_kv && i < p.S_q && (!p.causal || key <= i + off);
           });
       tc_fence_before_sync();
       __syncwarp();
@@ -353,20 +390,19 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&ctl->mma_done, 0, p.wait_limit_ns, p.err, 71));
     tc_fence_after_sync();
     const bool have = ok && n_steps > 0;
-    // dV into the V tile, dK (times scale) into the K tile: both are dead.
+    // dV into the V tile (group 0), dK times scale into the K tile (group 1):
+    // both tiles are dead.
 #pragma unroll 1
     for (int hh = 0; hh < 2; ++hh) {
       uint32_t o[64] = {};
-      if (have) tmem_ld64_wait(lane_addr + 256 + hh * 64, o);
-      stage_row<kBF16>(s_v, r, hh, o, 1.f);
-      if (have) tmem_ld64_wait(lane_addr + 384 + hh * 64, o);
-      stage_row<kBF16>(s_k, r, hh, o, p.scale);
+      if (have) tmem_ld64_wait(lane_addr + 256 + 128 * g + hh * 64, o);
+      stage_row<kBF16>(g == 0 ? s_v : s_k, r, hh, o, g == 0 ? 1.f : p.scale);
     }
     tc_fence_before_sync();
     __syncwarp();
     if (lane == 0) mbar_arrive(&ctl->tmem_free);
     fence_proxy_async_smem();
-    named_barrier_sync(1, 128);
+    named_barrier_sync(1, kEwWarps * 32);
     if (threadIdx.x == 0) {
       store_tile(&tm_dv, s_v, key0, h, b, p.bshd);
       store_tile(&tm_dk, s_k, key0, h, b, p.bshd);
@@ -415,9 +451,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       mbar_init(&ctl->empty[s], 1);
     }
     mbar_init(&ctl->mm_full, 1);
-    mbar_init(&ctl->ew_done, 4);
+    mbar_init(&ctl->ew_done, kEwWarps);
     mbar_init(&ctl->mma_done, 1);
-    mbar_init(&ctl->tmem_free, 4);
+    mbar_init(&ctl->tmem_free, kEwWarps);
     ctl->abort = 0;
     fence_mbar_init();
   }
@@ -427,7 +463,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   const uint32_t tmem = ctl->tmem_base;
   volatile int* abort_flag = &ctl->abort;
 
-  if (warp == kWarpLoad) {
+  if (warp >= kEwWarps) {
+   setmaxnreg_dec<kRegsCtl>();
+   if (warp == kWarpLoad) {
     if (lane == 0 && n_steps > 0) {
       mbar_arrive_expect_tx(&ctl->res_full, 2 * kTile);
       load_tile(s_q, &tm_q, &ctl->res_full, q0, h, b, p.bshd);
@@ -451,7 +489,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       mbar_wait(&ctl->res_full, 0, p.wait_limit_ns, p.err, 82);
     }
     __syncwarp();
-  } else if (warp == kWarpMmaB) {
+   } else if (warp == kWarpMmaB) {
     if (lane == 0 && n_steps > 0) {
       constexpr uint32_t id_s = idesc_f16(kBF16, kT, kT, false, false);
       constexpr uint32_t id_o = idesc_f16(kBF16, kT, kT, false, true);
@@ -481,10 +519,13 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     mbar_wait(&ctl->tmem_free, 0, p.wait_limit_ns, p.err, 87);
     tc_fence_after_sync();
     tmem_dealloc(tmem, 512);
+   }
   } else {
-    const int r = warp * 32 + lane;  // query row within the tile
+    setmaxnreg_inc<kRegsEw>();
+    const int g = warp / 4;                // column group of this warp
+    const int r = (warp % 4) * 32 + lane;  // query row within the tile
     const int i = q0 + r;
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
     const size_t ridx = static_cast<size_t>(bh) * p.S_q + i;
     const float lse2 = i < p.S_q ? p.lse[ridx] * kLog2e : 0.f;
     const float dlt = i < p.S_q ? p.delta[ridx] : 0.f;
@@ -497,10 +538,11 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       const bool full = k0 + kT <= p.S_kv && q0 + kT <= p.S_q &&
                         (!p.causal || k0 + kT - 1 <= q0 + off);
       elementwise_step<kBF16>(
-          lane_addr, 0, 128, p.scale_log2, [&](int) { return lse2; }, [&](int) { return dlt; },
-          [&](int col) {
+          lane_addr, g, 0, 128, p.scale_log2, !full, 2, [=](int) { return lse2; },
+          [=](int) { return dlt; },
+          [=](int col) {
             const int key = k0 + col;
-            return full || (key < p.S_kv && i < p.S_q && (!p.causal || key <= i + off));
+            return key < p.S_kv && i < p.S_q && (!p.causal || key <= i + off);
           });
       tc_fence_before_sync();
       __syncwarp();
@@ -510,17 +552,16 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&ctl->mma_done, 0, p.wait_limit_ns, p.err, 91));
     tc_fence_after_sync();
     const bool have = ok && n_steps > 0;
-#pragma unroll 1
-    for (int hh = 0; hh < 2; ++hh) {  // dQ (times scale) into the Q tile, dead now
+    {  // dQ times scale into the Q tile (dead now): columns [64g, 64g + 64)
       uint32_t o[64] = {};
-      if (have) tmem_ld64_wait(lane_addr + 256 + hh * 64, o);
-      stage_row<kBF16>(s_q, r, hh, o, p.scale);
+      if (have) tmem_ld64_wait(lane_addr + 256 + g * 64, o);
+      stage_row<kBF16>(s_q, r, g, o, p.scale);
     }
     tc_fence_before_sync();
     __syncwarp();
     if (lane == 0) mbar_arrive(&ctl->tmem_free);
     fence_proxy_async_smem();
-    named_barrier_sync(1, 128);
+    named_barrier_sync(1, kEwWarps * 32);
     if (threadIdx.x == 0) {
       store_tile(&tm_dq, s_q, q0, h, b, p.bshd);
       tma_store_commit();
@@ -532,6 +573,12 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 
 template <class K>
 cudaError_t configure(K kern) {
+  // The in-kernel register split assumes exactly kRegsLaunchB registers per
+  // thread at launch; with fewer, setmaxnreg.inc would never complete.
+  cudaFuncAttributes fa{};
+  cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != kRegsLaunchB) return cudaErrorInvalidConfiguration;
   return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemB);
 }
 
