@@ -47,10 +47,11 @@ constexpr int kWarpLoad = 8;
 constexpr int kWarpMmaB = 9;
 // Registers are granted per warpgroup: the block launches with 168 per
 // thread (64512 in all) and setmaxnreg gives the two element-wise warpgroups
-// 224, the control warpgroup 56 (2*128*224 + 128*56 = 64512).
+// 200, the control warpgroup 104 (2*128*200 + 128*104 = 64512): with less,
+// the MMA warp's unrolled issue loops spill.
 constexpr int kRegsLaunchB = 168;
-constexpr int kRegsEw = 224;
-constexpr int kRegsCtl = 56;
+constexpr int kRegsEw = 200;
+constexpr int kRegsCtl = 104;
 static_assert(2 * 128 * kRegsEw + 128 * kRegsCtl <= kThreadsB * kRegsLaunchB,
               "register split exceeds the block's launch allocation");
 constexpr int kRing = 2;                   // stages of the walking pair of tiles
@@ -144,9 +145,9 @@ __device__ __forceinline__ void stage_row(uint8_t* tile, int r, int h, const uin
 // Packed pairs of group 1 land on fp32 columns of group 0, so every
 // element-wise warp loads its columns before any of them stores (barrier
 // `bar_id` over all element-wise threads).  `lse2_of(c)` / `delta_of(c)` give
-// the row statistics for column c (dK/dV kernel: per query column; dQ kernel:
-// constant per row); `visible(c)` masks causal and ragged positions and is
-// only evaluated when `masked`.
+// the row statistics of the column pair (c, c + 1) as a float2 (dK/dV
+// kernel: per query column; dQ kernel: constant per row); `visible(c)` masks
+// causal and ragged positions and is only evaluated when `masked`.
 template <bool kBF16, bool kMasked, int kHalf, class Lse, class Delta, class Vis>
 __device__ __forceinline__ void ew_compute(const uint32_t (&x)[64], const uint32_t (&y)[64],
                                            uint32_t (&pp)[16], uint32_t (&dd)[16], int g,
@@ -154,13 +155,15 @@ __device__ __forceinline__ void ew_compute(const uint32_t (&x)[64], const uint32
 #pragma unroll
   for (int q = 16 * kHalf; q < 16 * kHalf + 16; ++q) {
     float pv[2], dv[2];
+    const int col0 = 64 * g + 2 * q;
+    const float2 l2 = lse2_of(col0), dl = delta_of(col0);  // columns col0, col0 + 1
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      const int col = 64 * g + 2 * q + e;
-      float pe = ex2_approx(__uint_as_float(x[2 * q + e]) * c - lse2_of(col));
+      const int col = col0 + e;
+      float pe = ex2_approx(fmaf(__uint_as_float(x[2 * q + e]), c, -(e ? l2.y : l2.x)));
       if constexpr (kMasked) pe = visible(col) ? pe : 0.f;
       pv[e] = pe;
-      dv[e] = pe * (__uint_as_float(y[2 * q + e]) - delta_of(col));
+      dv[e] = pe * (__uint_as_float(y[2 * q + e]) - (e ? dl.y : dl.x));
     }
     pp[q - 16 * kHalf] = pack2<kBF16>(pv[0], pv[1]);
     dd[q - 16 * kHalf] = pack2<kBF16>(dv[0], dv[1]);
@@ -375,8 +378,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       const bool full = key0 + kT <= p.S_kv && q0 + kT <= p.S_q &&
                         (!p.causal || key0 + kT - 1 <= q0 + off);
       elementwise_step<kBF16>(
-          lane_addr, g, 0, 128, p.scale_log2, !full, 2, [=](int col) { return lse2[col]; },
-          [=](int col) { return dlt[col]; },
+          lane_addr, g, 0, 128, p.scale_log2, !full, 2,
+          [=](int col) { return *reinterpret_cast<const float2*>(lse2 + col); },
+          [=](int col) { return *reinterpret_cast<const float2*>(dlt + col); },
           [=](int col) {
             const int i = q0 + col;
             return key < p.S_kv && i < p.S_q && (!p.causal || key <= i + off);
@@ -538,8 +542,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       const bool full = k0 + kT <= p.S_kv && q0 + kT <= p.S_q &&
                         (!p.causal || k0 + kT - 1 <= q0 + off);
       elementwise_step<kBF16>(
-          lane_addr, g, 0, 128, p.scale_log2, !full, 2, [=](int) { return lse2; },
-          [=](int) { return dlt; },
+          lane_addr, g, 0, 128, p.scale_log2, !full, 2,
+          [=](int) { return make_float2(lse2, lse2); },
+          [=](int) { return make_float2(dlt, dlt); },
           [=](int col) {
             const int key = k0 + col;
             return key < p.S_kv && i < p.S_q && (!p.causal || key <= i + off);
