@@ -25,7 +25,10 @@ are stated at the top of ``attn_oracle.c``:
   factors (Wave February 2025 Release, EvoFormer list, "FAv3 - FP8"), E4M3 decoded from the
   OCP 8-bit floating point definition;
 * backward: dQ, dK, dV of the prefill definition by the chain rule
-  (Wave February 2025 Release, EvoFormer list, "Backward Flash Attention").
+  (Wave February 2025 Release, EvoFormer list, "Backward Flash Attention");
+* FP8 MQA logits: sum over heads of w * ReLU(kv_scale * q.k) inside each
+  row's key window (aiter PR 7412, "FP8 MQA logits"; the formula is a
+  reading, stated in ``attn_oracle.c``).
 
 Every function here is pinned by ``tests/test_oracle.py`` against library
 routines, closed forms and analytic fixtures; no part is left unpinned.
@@ -93,6 +96,9 @@ def _load():
                                                    ctypes.c_int, ctypes.c_int, ctypes.c_double,
                                                    ctypes.c_int]
             lib.oracle_prefill_bwd_f64.restype = ctypes.c_int
+            lib.oracle_mqa_logits_f64.argtypes = [dp, dp, dp, dp, ip, ip, dp, L, L, L, L, L,
+                                                  ctypes.c_int, ctypes.c_int]
+            lib.oracle_mqa_logits_f64.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -271,3 +277,24 @@ def prefill_bwd(q, k, v, dout, *, causal: bool, scale: float, layout: int = BHSD
     if rc != 0:
         raise RuntimeError("oracle_prefill_bwd_f64 failed (rc=%d)" % rc)
     return dq, dk, dv
+
+
+def mqa_logits(q, kv, kv_scale, weights, start, end, *, clean_logits: bool, out=None,
+               n_threads: int | None = None):
+    """FP8 MQA logits in float64 (inputs already decoded to numbers):
+    ``q`` [S_q,H,D], ``kv`` [S_kv,D], ``kv_scale`` [S_kv], ``weights`` [S_q,H],
+    ``start``/``end`` [S_q] int32.  Returns logits [S_q,S_kv]; entries outside
+    a row's window are -inf with ``clean_logits``, else those of ``out``
+    (NaN if ``out`` is None)."""
+    q64, kv64, sc64, w64 = _f64(q), _f64(kv), _f64(kv_scale), _f64(weights)
+    st, en = _i32(start), _i32(end)
+    S_q, H, D = q64.shape
+    S_kv = kv64.shape[0]
+    res = np.full((S_q, S_kv), np.nan) if out is None else np.array(_f64(out), copy=True)
+    rc = _load().oracle_mqa_logits_f64(_dptr(q64), _dptr(kv64), _dptr(sc64), _dptr(w64),
+                                       _iptr(st), _iptr(en), _dptr(res), S_q, S_kv, H, D, S_kv,
+                                       int(bool(clean_logits)),
+                                       int(n_threads or default_threads()))
+    if rc != 0:
+        raise RuntimeError("oracle_mqa_logits_f64 failed (rc=%d)" % rc)
+    return res

@@ -64,6 +64,17 @@
  *     dQ_i  = scale sum_j dS_ij k_j,   dK_j = scale sum_i dS_ij q_i
  * over the visible (i, j) pairs.
  *
+ * FP8 MQA logits ("[FlyDSL] FP8 MQA logits improvements for gfx950", aiter
+ * PR 7412: Summary; Changes/Kernel head_acc, rs_head, lds_scales; Test
+ * windows causal/cp/misaligned/empty/past_end; clean_logits).  The page names
+ * the pieces but prints no formula; the reading taken: one K row per key
+ * shared by all heads (multi-query), a per-head score, a nonlinearity (ReLU)
+ * between the per-head products and the weighted head reduction (without it
+ * the head sum would collapse into one product), and a per-key scale:
+ *     logits[i,j] = sum_h w[i,h] * max(0, kv_scale[j] * (q[i,h] . k[j]))
+ * for j in row i's window [start_i, end_i) clamped to [0, S_kv); outside it
+ * the entry is -inf when clean_logits is set and left untouched otherwise.
+ *
  * Rows are independent; they are spread over POSIX threads.
  */
 #include <math.h>
@@ -486,4 +497,55 @@ int oracle_prefill_bwd_f64(const double *q, const double *k, const double *v,
     if (B == 0 || H == 0) return 0;
     bwd_job J = {q, k, v, dout, dq, dk, dv, B, H, S_q, S_kv, D, layout, causal, scale, 0};
     return run_threads(bwd_worker, &J, n_threads);
+}
+
+/* ------------------------------------------------------------- MQA logits */
+
+typedef struct {
+    const double *q, *kv, *kv_scale, *w;
+    const int32_t *start, *end;
+    double *logits;
+    long S_q, S_kv, H, D, stride;
+    int clean;
+    long next_row;
+} mqa_job;
+
+static void *mqa_worker(void *arg) {
+    mqa_job *J = (mqa_job *)arg;
+    for (;;) {
+        long i = __atomic_fetch_add(&J->next_row, 1, __ATOMIC_RELAXED);
+        if (i >= J->S_q) break;
+        long lo = J->start[i] < 0 ? 0 : J->start[i];
+        long hi = J->end[i] > J->S_kv ? J->S_kv : J->end[i];
+        double *row = J->logits + i * J->stride;
+        for (long j = 0; j < J->S_kv; ++j) {
+            if (j < lo || j >= hi) {
+                if (J->clean) row[j] = -INFINITY;
+                continue;
+            }
+            double acc = 0.0;
+            for (long h = 0; h < J->H; ++h) {
+                const double *q_row = J->q + (i * J->H + h) * J->D;
+                double dot = 0.0;
+                for (long d = 0; d < J->D; ++d) dot += q_row[d] * J->kv[j * J->D + d];
+                const double s = J->kv_scale[j] * dot;
+                acc += J->w[i * J->H + h] * (s > 0.0 ? s : 0.0);
+            }
+            row[j] = acc;
+        }
+    }
+    return NULL;
+}
+
+/* q: [S_q, H, D]; kv: [S_kv, D]; kv_scale: [S_kv]; w: [S_q, H]; start, end:
+ * [S_q] int32; logits: [S_q, stride] (stride >= S_kv), written as above.
+ * Returns 0, or -1 on bad arguments. */
+int oracle_mqa_logits_f64(const double *q, const double *kv, const double *kv_scale,
+                          const double *w, const int32_t *start, const int32_t *end,
+                          double *logits, long S_q, long S_kv, long H, long D, long stride,
+                          int clean, int n_threads) {
+    if (S_q < 0 || S_kv < 0 || H <= 0 || D <= 0 || stride < S_kv) return -1;
+    if (S_q == 0) return 0;
+    mqa_job J = {q, kv, kv_scale, w, start, end, logits, S_q, S_kv, H, D, stride, clean, 0};
+    return run_threads(mqa_worker, &J, n_threads);
 }

@@ -502,6 +502,57 @@ def test_prefill_bwd_invariants():
     np.testing.assert_array_equal(dv, dv2)
 
 
+# ------------------------------------------------------------- MQA logits
+
+
+def _mqa_torch(q8, kv8, kv_scale, w, start, end, clean):
+    """PyTorch float64: per-head scores by einsum, ReLU, weighted head sum,
+    window mask."""
+    q = q8.double()
+    k = kv8.double()
+    s = torch.einsum("ihd,jd->ihj", q, k) * kv_scale.double()[None, None, :]
+    out = (torch.relu(s) * w.double()[:, :, None]).sum(dim=1)
+    j = torch.arange(k.shape[0])[None, :]
+    inside = (j >= start.long()[:, None].clamp(min=0)) & (j < end.long()[:, None])
+    fill = float("-inf") if clean else float("nan")
+    return torch.where(inside, out, torch.full_like(out, fill))
+
+
+@pytest.mark.parametrize("window", ["causal", "cp", "misaligned", "empty", "past_end"])
+@pytest.mark.parametrize("clean", [True, False])
+def test_mqa_logits_matches_torch(window, clean):
+    case = workloads.MqaCase("t", 23, 70, 8, 32, window, clean, seed=91)
+    q8, kv8, sc, w, st, en = workloads.make_mqa(case)
+    ours = oracle.mqa_logits(oracle.decode_e4m3(q8), oracle.decode_e4m3(kv8), sc, w, st, en,
+                             clean_logits=clean)
+    ref = _mqa_torch(q8, kv8, sc, w, st, en, clean).numpy()
+    np.testing.assert_array_equal(np.isnan(ours), np.isnan(ref))
+    np.testing.assert_array_equal(np.isneginf(ours), np.isneginf(ref))
+    fin = np.isfinite(ref)
+    np.testing.assert_allclose(ours[fin], ref[fin], rtol=1e-12, atol=1e-12)
+
+
+def test_mqa_logits_closed_forms():
+    """Zero weights give 0 inside the window; a head whose query is the
+    negated key contributes nothing (ReLU); an empty or past-the-end window
+    leaves the row all -inf (clean) or untouched."""
+    S_q, S_kv, H, D = 3, 5, 2, 4
+    k = np.arange(S_kv * D, dtype=np.float64).reshape(S_kv, D) / 10.0
+    q = np.zeros((S_q, H, D))
+    q[:, 0, :] = k[1]     # head 0 aligned with key 1
+    q[:, 1, :] = -k[1]    # head 1 opposed: ReLU removes it
+    sc = np.full(S_kv, 0.5)
+    w = np.array([[2.0, 7.0]] * S_q)
+    start = np.array([0, 2, 5], dtype=np.int32)
+    end = np.array([5, 2, 9], dtype=np.int32)
+    out = oracle.mqa_logits(q, k, sc, w, start, end, clean_logits=True)
+    assert out[0, 1] == 2.0 * 0.5 * float(k[1] @ k[1])
+    assert np.all(np.isneginf(out[1])) and np.all(np.isneginf(out[2]))
+    out = oracle.mqa_logits(q, k, sc, np.zeros_like(w), start, end, clean_logits=False,
+                            out=np.full((S_q, S_kv), 3.0))
+    assert np.all(out[0] == 0.0) and np.all(out[1:] == 3.0)
+
+
 # --------------------------------------------------------- planted mistakes
 
 _MUTANTS = {
@@ -528,6 +579,9 @@ _MUTANTS = {
     "bwd_dk_from_k": ("dk_row[d] += J->scale * ds * q_row[d];",
                       "dk_row[d] += J->scale * ds * k_row[d];"),
     "bwd_dv_from_ds": ("dv_row[d] += p[j] * do_row[d];", "dv_row[d] += ds * do_row[d];"),
+    "mqa_no_relu": ("acc += J->w[i * J->H + h] * (s > 0.0 ? s : 0.0);",
+                    "acc += J->w[i * J->H + h] * s;"),
+    "mqa_window_inclusive": ("if (j < lo || j >= hi) {", "if (j < lo || j > hi) {"),
     "e4m3_bias_8": ("ldexp(1.0 + (double)m / 8.0, e - 7)", "ldexp(1.0 + (double)m / 8.0, e - 8)"),
     "e4m3_subnormal_as_normal": ("v = ldexp((double)m / 8.0, -6);",
                                  "v = ldexp(1.0 + (double)m / 8.0, -7);"),
@@ -543,6 +597,8 @@ def _pins_pass() -> bool:
         lambda: test_extend_matches_torch_sdpa(True, 8, 2, 8),
         lambda: test_e4m3_decode_matches_torch_for_every_code(),
         lambda: test_prefill_bwd_matches_torch_autograd(9, 30, True, "bshd"),
+        lambda: test_mqa_logits_matches_torch("misaligned", True),
+        lambda: test_mqa_logits_closed_forms(),
     ] + [lambda p=p: test_golden_fixture(p)
          for p in sorted(glob.glob(os.path.join(GOLDEN, "*.json")))]
     for c in checks:
@@ -580,6 +636,8 @@ def test_mutants_are_caught(name):
         mutant.oracle_e4m3_decode.restype = None
         mutant.oracle_prefill_bwd_f64.argtypes = saved.oracle_prefill_bwd_f64.argtypes
         mutant.oracle_prefill_bwd_f64.restype = ctypes.c_int
+        mutant.oracle_mqa_logits_f64.argtypes = saved.oracle_mqa_logits_f64.argtypes
+        mutant.oracle_mqa_logits_f64.restype = ctypes.c_int
         oracle._lib = mutant
         try:
             assert not _pins_pass(), "pins did not catch planted mistake %r" % name

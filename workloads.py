@@ -26,6 +26,10 @@ Recipe (every draw uses a CPU ``torch.Generator`` seeded with ``seed``):
   codes are ``(x / descale)`` rounded by PyTorch's float8_e4m3fn conversion
   (round to nearest even).  The codes and the three descale factors are the
   inputs; nothing of the attention arithmetic happens here.
+* FP8 MQA logits: q ``randn`` [S_q,H,D] rounded to E4M3 (no separate scale),
+  then kv ``randn`` [S_kv,D] quantized per row (kv_scale[j] = max|row|/448,
+  codes = row / kv_scale), then weights ``randn`` [S_q,H] / sqrt(H) in
+  float32, then the windows of the chosen kind (below, in ``mqa_windows``).
 * extend (prefill of new tokens against a paged cache): first the cached
   prefix lengths (``randint`` uniform on [prefix_min, prefix_max]) unless
   given, ``kv_len_b = prefix_b + S_q``; then Q [B,S_q,H_q,D]; then per
@@ -187,6 +191,29 @@ C7 = Fp8PrefillCase("prefill_fp8e4m3_bhsd_b4_h32_s4096_d128", 4, 32, 4096, 4096,
                     False)
 C7_CAUSAL = Fp8PrefillCase("prefill_fp8e4m3_bhsd_b4_h32_s4096_d128_causal", 4, 32, 4096, 4096,
                            128, "bhsd", True)
+
+@dataclass(frozen=True)
+class MqaCase:
+    """FP8 MQA logits: S_q query rows of H heads against S_kv shared keys."""
+    name: str
+    S_q: int
+    S_kv: int
+    H: int
+    D: int
+    window: str  # causal | cp | misaligned | empty | past_end
+    clean_logits: bool = True
+    seed: int = 0
+
+    def flops(self, start, end) -> float:
+        """2*H*D per in-window (row, key) pair (the per-head dot products)."""
+        lo = start.clamp(min=0)
+        hi = end.clamp(max=self.S_kv)
+        return 2.0 * self.H * self.D * float((hi - lo).clamp(min=0).sum())
+
+
+# Long-context indexer shape of the page's sweep (2048 x 131072 is its largest;
+# this one keeps the output at 1 GB): 1024 rows x 65536 keys, 64 heads, D=128.
+C9 = MqaCase("mqa_logits_fp8_sq1024_skv65536_h64_d128_causal", 1024, 65536, 64, 128, "causal")
 
 # Prefix-cached prefill: 8 requests of 1024 new tokens each on top of cached
 # prefixes of up to 15360 tokens, Llama-3-8B-like GQA heads, 16-token pages.
@@ -385,3 +412,48 @@ def make_extend(case: ExtendCase, prefix_lens=None) -> ExtendInputs:
     k, v, pt = _place_pages(g, rows_k, rows_v, kv_lens, case.page_size, case.max_pages,
                             case.H_kv, case.D, dt)
     return ExtendInputs(q, k, v, kv_lens.to(torch.int32), pt, case.page_size, case.max_pages)
+
+
+def mqa_windows(kind: str, S_q: int, S_kv: int, g: torch.Generator):
+    """[start, end) per query row for the window kinds of the MQA-logits
+    sweep; `g` draws the random ones.
+      causal:     [0, i + S_kv - S_q + 1)            (bottom-right)
+      cp:         the second half of the causal window (a context-parallel
+                  shard that sees a suffix of its prefix)
+      misaligned: random start <= end inside [0, S_kv], not tile-aligned
+      empty:      end == start (random start)
+      past_end:   start >= S_kv
+    """
+    i = torch.arange(S_q, dtype=torch.int64)
+    causal_end = (i + S_kv - S_q + 1).clamp(min=0, max=S_kv)
+    if kind == "causal":
+        start, end = torch.zeros_like(i), causal_end
+    elif kind == "cp":
+        start, end = causal_end // 2, causal_end
+    elif kind == "misaligned":
+        a = torch.randint(0, S_kv + 1, (S_q,), generator=g)
+        b = torch.randint(0, S_kv + 1, (S_q,), generator=g)
+        start, end = torch.minimum(a, b), torch.maximum(a, b)
+    elif kind == "empty":
+        start = torch.randint(0, S_kv + 1, (S_q,), generator=g)
+        end = start.clone()
+    elif kind == "past_end":
+        start = S_kv + torch.randint(0, 64, (S_q,), generator=g)
+        end = start + torch.randint(0, 64, (S_q,), generator=g)
+    else:
+        raise ValueError(kind)
+    return start.to(torch.int32), end.to(torch.int32)
+
+
+def make_mqa(case: MqaCase):
+    """Return (q8 [S_q,H,D] e4m3, kv8 [S_kv,D] e4m3, kv_scale [S_kv] f32,
+    weights [S_q,H] f32, start, end [S_q] int32) on the CPU."""
+    g = _gen(case.seed)
+    q8 = torch.randn((case.S_q, case.H, case.D), generator=g).to(torch.float8_e4m3fn)
+    kv = torch.randn((case.S_kv, case.D), generator=g)
+    amax = kv.abs().amax(dim=1).clamp(min=1e-6)
+    kv_scale = (amax / 448.0).to(torch.float32)
+    kv8 = (kv / kv_scale[:, None]).to(torch.float8_e4m3fn)
+    w = torch.randn((case.S_q, case.H), generator=g) / math.sqrt(case.H)
+    start, end = mqa_windows(case.window, case.S_q, case.S_kv, g)
+    return q8, kv8, kv_scale, w.to(torch.float32), start, end
