@@ -43,7 +43,7 @@ _STATUS_NAMES = {
 }
 
 # Names the header exports (checked against include/attn_gb300.h by the tests).
-EXPORTED = ("attn_prefill_fwd", "attn_prefill_bwd", "attn_prefill_fp8_fwd", "attn_extend_fwd", "attn_decode_fwd", "attn_decode_fwd_noalloc",
+EXPORTED = ("attn_prefill_fwd", "attn_prefill_bwd", "attn_mqa_logits_fp8", "attn_prefill_fp8_fwd", "attn_extend_fwd", "attn_decode_fwd", "attn_decode_fwd_noalloc",
             "attn_last_error",
             "attn_device_error", "attn_set_wait_limit_ns", "attn_release_workspace",
             "attn_version")
@@ -77,6 +77,8 @@ def lib() -> ctypes.CDLL:
             L.attn_prefill_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, cf,
                                            vp]
             L.attn_prefill_fwd.restype = ci
+            L.attn_mqa_logits_fp8.argtypes = [vp] * 7 + [ci] * 4 + [ctypes.c_int64, ci, vp]
+            L.attn_mqa_logits_fp8.restype = ci
             L.attn_prefill_bwd.argtypes = [vp] * 10 + [ci] * 8 + [cf, vp]
             L.attn_prefill_bwd.restype = ci
             L.attn_prefill_fp8_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci,
@@ -122,6 +124,13 @@ def attn_prefill_fwd(q, k, v, o, lse, B, H, S_q, S_kv, D, layout, dtype, causal,
     """C ``attn_prefill_fwd``; pointers and stream as ints.  Returns the status."""
     return lib().attn_prefill_fwd(q, k, v, o, lse, B, H, S_q, S_kv, D, layout, dtype, causal,
                                   scale, stream)
+
+
+def attn_mqa_logits_fp8(q, kv, kv_scale, weights, window_start, window_end, logits, S_q, S_kv,
+                        H, D, logits_stride, clean_logits, stream) -> int:
+    """C ``attn_mqa_logits_fp8``; pointers and stream as ints.  Returns the status."""
+    return lib().attn_mqa_logits_fp8(q, kv, kv_scale, weights, window_start, window_end, logits,
+                                     S_q, S_kv, H, D, logits_stride, clean_logits, stream)
 
 
 def attn_prefill_bwd(q, k, v, o, dout, lse, dq, dk, dv, delta, B, H, S_q, S_kv, D, layout,
@@ -252,6 +261,28 @@ def prefill(q, k, v, *, causal: bool = False, scale: float | None = None,
                             code, _dtype_code(q), int(bool(causal)), float(scale),
                             _stream_handle(stream)))
     return (out, lse) if return_lse else out
+
+
+def mqa_logits_fp8(q, kv, kv_scale, weights, window_start, window_end, *,
+                   clean_logits: bool = True, out=None, stream=None):
+    """FP8 MQA logits over torch CUDA tensors: ``q`` [S_q,H,D] and ``kv``
+    [S_kv,D] E4M3 (float8_e4m3fn or uint8 codes), ``kv_scale`` [S_kv] and
+    ``weights`` [S_q,H] fp32, windows [S_q] int32.  Returns fp32 logits
+    [S_q,S_kv] (``out`` may be a preallocated [S_q, >= S_kv] fp32 tensor)."""
+    torch = _torch()
+    _require_cuda(q, kv, kv_scale, weights, window_start, window_end)
+    S_q, H, D = q.shape
+    S_kv = kv.shape[0]
+    if out is None:
+        out = torch.empty((S_q, S_kv), device=q.device, dtype=torch.float32)
+    if (not out.is_cuda or out.dtype != torch.float32 or out.dim() != 2 or out.stride(1) != 1
+            or tuple(out.shape) != (S_q, S_kv)):
+        raise ValueError("out must be a CUDA float32 [S_q, S_kv] tensor with unit column stride")
+    _check(attn_mqa_logits_fp8(q.data_ptr(), kv.data_ptr(), kv_scale.data_ptr(),
+                               weights.data_ptr(), window_start.data_ptr(),
+                               window_end.data_ptr(), out.data_ptr(), S_q, S_kv, H, D,
+                               out.stride(0), int(bool(clean_logits)), _stream_handle(stream)))
+    return out
 
 
 def prefill_bwd(q, k, v, o, dout, lse, *, causal: bool = False, scale: float | None = None,
@@ -408,4 +439,4 @@ def check_device_error() -> None:
 
 
 __all__ = [n for n in dir() if n.startswith(("attn_", "ATTN_"))] + [
-    "AttnError", "prefill", "prefill_bwd", "prefill_fp8", "extend", "decode", "lib", "library_path", "check_device_error", "EXPORTED"]
+    "AttnError", "prefill", "prefill_bwd", "mqa_logits_fp8", "prefill_fp8", "extend", "decode", "lib", "library_path", "check_device_error", "EXPORTED"]

@@ -15,6 +15,7 @@
 #include "../../include/attn_gb300.h"
 #include "backward_sm103a.h"
 #include "decode_sm103a.h"
+#include "mqa_logits_sm103a.h"
 #include "prefill_sm103a.h"
 #include "tmap.h"
 
@@ -258,6 +259,73 @@ attn_status attn_prefill_fwd(const void* q, const void* k, const void* v, void* 
   p.wait_limit_ns = g_wait_limit_ns.load();
   cudaError_t e = attn_sm103a::prefill_launch(mq, mk, mv, mo, p, D, bf16, stream);
   if (e != cudaSuccess) return fail_cuda(e, "prefill launch");
+  return ATTN_OK;
+}
+
+attn_status attn_mqa_logits_fp8(const void* q, const void* kv, const float* kv_scale,
+                                const float* weights, const int32_t* window_start,
+                                const int32_t* window_end, float* logits, int S_q, int S_kv,
+                                int H, int D, int64_t logits_stride, int clean_logits,
+                                cudaStream_t stream) {
+  if (S_q < 0 || S_kv < 0) return fail(ATTN_ERR_INVALID_ARG, "S_q and S_kv must be >= 0");
+  if (H != 32 && H != 64 && H != 128)
+    return fail(ATTN_ERR_UNSUPPORTED, "H must be 32, 64 or 128");
+  if (D != 128) return fail(ATTN_ERR_UNSUPPORTED, "D must be 128");
+  if (clean_logits != 0 && clean_logits != 1)
+    return fail(ATTN_ERR_INVALID_ARG, "clean_logits must be 0 or 1");
+  if (logits_stride < S_kv) return fail(ATTN_ERR_INVALID_ARG, "logits_stride must be >= S_kv");
+  if (static_cast<int64_t>(S_q) * S_kv == 0) return ATTN_OK;
+  if (!q || !kv || !kv_scale || !weights || !window_start || !window_end || !logits)
+    return fail(ATTN_ERR_INVALID_ARG, "every pointer must be non-NULL");
+  if (!aligned16(q) || !aligned16(kv))
+    return fail(ATTN_ERR_INVALID_ARG, "q and kv must be 16-byte aligned");
+  if (static_cast<int64_t>(S_q) * H + 256 > 0x7FFFFFFF || S_kv > 0x7FFFFF00)
+    return fail(ATTN_ERR_UNSUPPORTED, "too many rows for one TMA descriptor");
+
+  DeviceState* st = nullptr;
+  attn_status s = device_state(&st);
+  if (s != ATTN_OK) return s;
+
+  CUtensorMap mq, mk;
+  {
+    uint64_t dims[2] = {static_cast<uint64_t>(D), static_cast<uint64_t>(S_q) * H};
+    uint64_t strides[1] = {static_cast<uint64_t>(D)};
+    uint32_t box[2] = {128, 256};
+    if (!attn_host::encode_tiled_8bit(&mq, q, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed for q");
+  }
+  {
+    uint64_t dims[2] = {static_cast<uint64_t>(D), static_cast<uint64_t>(S_kv)};
+    uint64_t strides[1] = {static_cast<uint64_t>(D)};
+    uint32_t box[2] = {128, static_cast<uint32_t>(attn_sm103a::mqa_keys_per_cta())};
+    if (!attn_host::encode_tiled_8bit(&mk, kv, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed for kv");
+  }
+  attn_sm103a::MqaParams p{};
+  p.kv_scale = kv_scale;
+  p.w = weights;
+  p.start = window_start;
+  p.end = window_end;
+  p.logits = logits;
+  p.stride = logits_stride;
+  p.S_q = S_q;
+  p.S_kv = S_kv;
+  p.H = H;
+  p.clean = clean_logits;
+  // Enough query groups per CTA to amortize loading the key tile, few enough
+  // that short key ranges still give every SM work.
+  const int groups = (S_q + attn_sm103a::mqa_rows_per_group(H) - 1) /
+                     attn_sm103a::mqa_rows_per_group(H);
+  const int64_t key_tiles = (S_kv + attn_sm103a::mqa_keys_per_cta() - 1) /
+                            attn_sm103a::mqa_keys_per_cta();
+  int per = 16;
+  while (per > 1 && key_tiles * ((groups + per - 1) / per) < 2 * st->num_sms) per /= 2;
+  p.groups_per_cta = per;
+  if ((groups + per - 1) / per > 65535) return fail(ATTN_ERR_UNSUPPORTED, "S_q too large");
+  p.err = st->err_word;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  cudaError_t e = attn_sm103a::mqa_logits_launch(mq, mk, p, stream);
+  if (e != cudaSuccess) return fail_cuda(e, "MQA logits launch");
   return ATTN_OK;
 }
 

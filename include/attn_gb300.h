@@ -83,6 +83,33 @@ ATTN_API attn_status attn_prefill_fwd(const void* q, const void* k, const void* 
                              attn_dtype dtype, int causal, float scale, cudaStream_t stream);
 
 /*
+ * FP8 MQA logits (the indexer-style op of aiter PR 7412, "[FlyDSL] FP8 MQA
+ * logits improvements for gfx950"; the page names its parts but prints no
+ * formula, and this is the reading taken):
+ *
+ *   logits[i,j] = sum_h weights[i,h] * max(0, kv_scale[j] * (q[i,h] . kv[j]))
+ *
+ * for j in row i's window [window_start[i], window_end[i]) clamped to
+ * [0, S_kv); outside it logits[i,j] = -inf if clean_logits, else untouched.
+ *
+ *   q             [S_q, H, D] E4M3 codes (torch.float8_e4m3fn)
+ *   kv            [S_kv, D] E4M3 codes, one key row shared by every head
+ *   kv_scale      [S_kv] fp32 per-key scale
+ *   weights       [S_q, H] fp32
+ *   window_start, [S_q] int32 on the device; any values (empty and
+ *   window_end    past-the-end windows are fine)
+ *   logits        [S_q, logits_stride] fp32 output, logits_stride >= S_kv
+ *   H             32, 64 or 128; D = 128 (else ATTN_ERR_UNSUPPORTED).
+ * Products are exact (E4M3 x E4M3) and accumulated in fp32.  Allocates
+ * nothing.
+ */
+ATTN_API attn_status attn_mqa_logits_fp8(const void* q, const void* kv, const float* kv_scale,
+                                         const float* weights, const int32_t* window_start,
+                                         const int32_t* window_end, float* logits, int S_q,
+                                         int S_kv, int H, int D, int64_t logits_stride,
+                                         int clean_logits, cudaStream_t stream);
+
+/*
  * Attention backward: gradients of attn_prefill_fwd's O.
  *
  * Defines, for the upstream gradient dO of O and P the softmax of the

@@ -111,6 +111,32 @@ def test_decode_empty_batch_is_a_no_op():
     assert _decode(B=0, num_pages=0) == attn.ATTN_OK
 
 
+def _mqa(**kw):
+    a = dict(q=16, kv=16, kv_scale=16, weights=16, window_start=16, window_end=16, logits=16,
+             S_q=4, S_kv=8, H=64, D=128, logits_stride=8, clean_logits=1, stream=None)
+    a.update(kw)
+    return attn.attn_mqa_logits_fp8(**a)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(H=48), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(D=64), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(S_q=-1), attn.ATTN_ERR_INVALID_ARG),
+    (dict(logits_stride=7), attn.ATTN_ERR_INVALID_ARG),
+    (dict(clean_logits=2), attn.ATTN_ERR_INVALID_ARG),
+    (dict(window_end=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(kv=8), attn.ATTN_ERR_INVALID_ARG),  # misaligned
+])
+def test_mqa_logits_rejects_bad_arguments(kw, code):
+    assert _mqa(**kw) == code
+    assert attn.attn_last_error()
+
+
+def test_mqa_logits_empty_problem_is_a_no_op():
+    assert _mqa(S_q=0, q=None) == attn.ATTN_OK
+    assert _mqa(S_kv=0, logits_stride=0) == attn.ATTN_OK
+
+
 def _bwd(**kw):
     a = dict(q=16, k=16, v=16, o=16, dout=16, lse=16, dq=16, dk=16, dv=16, delta=16, B=1, H=1,
              S_q=8, S_kv=8, D=128, layout=0, dtype=1, causal=0, scale=0.1, stream=None)
