@@ -17,7 +17,8 @@
 // rows' windows all miss the key tile is neither loaded nor multiplied (the
 // page's tile_skip / empty-window fix); with clean_logits its entries are
 // still filled with -inf.  Eight epilogue warps split each group's query
-// rows; their stores run along the key axis, so every warp writes 128
+// rows (a warp's rows own 128 contiguous tensor-memory columns, read with one
+// load); their stores run along the key axis, so every warp writes 128
 // contiguous bytes per row.  Every wait is bounded.
 #include "mqa_logits_sm103a.h"
 #include "sm103a_ptx.cuh"
@@ -111,10 +112,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&ctl->k_full, kKTile);
         tma_load_2d(smem, &tm_k, &ctl->k_full, 0, key0);
       }
+      // A group's windows and weights come from global memory; they are
+      // loaded one group ahead, before the wait for the ring slot, so their
+      // latency hides behind it instead of serializing the producer.
+      constexpr int kWPerLane = kN / 32;
+      int nlo = 0, nhi = 0;
+      float nw[kWPerLane];
+      auto fetch = [&](int u) {
+        const int i0 = (g_begin + u) * G;
+        nlo = nhi = 0;
+        if (lane < G && i0 + lane < p.S_q) {
+          nlo = p.start[i0 + lane];
+          nhi = p.end[i0 + lane];
+        }
+#pragma unroll
+        for (int e = 0; e < kWPerLane; ++e) {
+          const int c = lane + 32 * e;
+          const int i = i0 + c / H;
+          nw[e] = i < p.S_q ? p.w[static_cast<size_t>(i) * H + c % H] : 0.f;
+        }
+      };
+      fetch(0);
       int issued = 0;
       for (int u = 0; u < n_u; ++u) {
         if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
         const int st = u % kRing;
+        const int i0 = (g_begin + u) * G;
+        int lo = max(nlo, 0), hi = min(nhi, p.S_kv);
+        float w[kWPerLane];
+#pragma unroll
+        for (int e = 0; e < kWPerLane; ++e) w[e] = nw[e];
+        if (u + 1 < n_u) fetch(u + 1);
         bool ok = true;
         if (lane == 0 && u >= kRing)
           ok = mbar_wait(&ctl->empty[st], (u / kRing - 1) & 1, p.wait_limit_ns, p.err, 150);
@@ -123,24 +151,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         Stage& sg = stages[st];
-        const int i0 = (g_begin + u) * G;
         bool live = false;
         if (lane < G) {
-          const int i = i0 + lane;
-          int lo = 0, hi = 0;
-          if (i < p.S_q) {
-            lo = max(p.start[i], 0);
-            hi = min(p.end[i], p.S_kv);
-          }
+          if (i0 + lane >= p.S_q) lo = hi = 0;
           sg.lo[lane] = lo;
           sg.hi[lane] = hi;
           live = lo < hi && lo < key0 + kKeys && hi > key0;
         }
         live = __any_sync(0xffffffffu, live);
-        for (int c = lane; c < kN; c += 32) {
-          const int i = i0 + c / H;
-          sg.w[c] = i < p.S_q ? p.w[static_cast<size_t>(i) * H + c % H] : 0.f;
-        }
+#pragma unroll
+        for (int e = 0; e < kWPerLane; ++e) sg.w[lane + 32 * e] = w[e];
         if (lane == 0) sg.live = live ? 1 : 0;
         __syncwarp();
         if (lane == 0) {
@@ -209,25 +229,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Stage& sg = stages[st];
       const bool live = sg.live != 0;
       const int i0 = (g_begin + u) * G;
-#pragma unroll 1
-      for (int g = half * (G / 2); g < (half + 1) * (G / 2); ++g) {
+      // This warp's rows of the group own 128 contiguous columns of the
+      // buffer: one load, one wait.
+      float sv[128];
+      if (live) tmem_ld128_wait(lane_addr + 256 * b + 128 * half, sv);
+      const uint64_t sc2 = f2_pack(scale, scale);
+#pragma unroll
+      for (int gg = 0; gg < G / 2; ++gg) {
+        const int g = half * (G / 2) + gg;
         const int i = i0 + g;
         float acc = 0.f;
         if (live) {
+          uint64_t a0 = f2_pack(0.f, 0.f), a1 = a0;
 #pragma unroll
-          for (int h0 = 0; h0 < H; h0 += 32) {
-            float sv[32];
-            tmem_ld32_wait(lane_addr + 256 * b + g * H + h0,
-                           reinterpret_cast<uint32_t(&)[32]>(sv));
-#pragma unroll
-            for (int c = 0; c < 32; c += 4) {
-              const float4 w4 = *reinterpret_cast<const float4*>(&sg.w[g * H + h0 + c]);
-              acc = fmaf(fmaxf(sv[c] * scale, 0.f), w4.x, acc);
-              acc = fmaf(fmaxf(sv[c + 1] * scale, 0.f), w4.y, acc);
-              acc = fmaf(fmaxf(sv[c + 2] * scale, 0.f), w4.z, acc);
-              acc = fmaf(fmaxf(sv[c + 3] * scale, 0.f), w4.w, acc);
-            }
+          for (int c = 0; c < H; c += 4) {
+            const float4 w4 = *reinterpret_cast<const float4*>(&sg.w[g * H + c]);
+            float x0, x1, x2, x3;
+            f2_unpack(f2_mul(f2_pack(sv[gg * H + c], sv[gg * H + c + 1]), sc2), x0, x1);
+            f2_unpack(f2_mul(f2_pack(sv[gg * H + c + 2], sv[gg * H + c + 3]), sc2), x2, x3);
+            a0 = f2_fma(f2_pack(fmaxf(x0, 0.f), fmaxf(x1, 0.f)), f2_pack(w4.x, w4.y), a0);
+            a1 = f2_fma(f2_pack(fmaxf(x2, 0.f), fmaxf(x3, 0.f)), f2_pack(w4.z, w4.w), a1);
           }
+          float p0, p1, p2, p3;
+          f2_unpack(a0, p0, p1);
+          f2_unpack(a1, p2, p3);
+          acc = (p0 + p1) + (p2 + p3);
         }
         if (i < p.S_q && j < p.S_kv) {
           const bool inside = j >= sg.lo[g] && j < sg.hi[g];
