@@ -279,7 +279,8 @@ attn_status attn_mqa_logits_fp8(const void* q, const void* kv, const float* kv_s
     return fail(ATTN_ERR_INVALID_ARG, "every pointer must be non-NULL");
   if (!aligned16(q) || !aligned16(kv))
     return fail(ATTN_ERR_INVALID_ARG, "q and kv must be 16-byte aligned");
-  if (static_cast<int64_t>(S_q) * H + 256 > 0x7FFFFFFF || S_kv > 0x7FFFFF00)
+  if ((static_cast<int64_t>(S_q) + attn_sm103a::mqa_rows_per_block(H)) * H > 0x7FFFFFFF ||
+      S_kv > 0x7FFFFF00)
     return fail(ATTN_ERR_UNSUPPORTED, "too many rows for one TMA descriptor");
 
   DeviceState* st = nullptr;
@@ -290,14 +291,14 @@ attn_status attn_mqa_logits_fp8(const void* q, const void* kv, const float* kv_s
   {
     uint64_t dims[2] = {static_cast<uint64_t>(D), static_cast<uint64_t>(S_q) * H};
     uint64_t strides[1] = {static_cast<uint64_t>(D)};
-    uint32_t box[2] = {128, 256};
+    uint32_t box[2] = {128, static_cast<uint32_t>(attn_sm103a::mqa_rows_per_slab_box())};
     if (!attn_host::encode_tiled_8bit(&mq, q, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed for q");
   }
   {
     uint64_t dims[2] = {static_cast<uint64_t>(D), static_cast<uint64_t>(S_kv)};
     uint64_t strides[1] = {static_cast<uint64_t>(D)};
-    uint32_t box[2] = {128, static_cast<uint32_t>(attn_sm103a::mqa_keys_per_cta())};
+    uint32_t box[2] = {128, static_cast<uint32_t>(attn_sm103a::mqa_keys_per_tile())};
     if (!attn_host::encode_tiled_8bit(&mk, kv, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed for kv");
   }
@@ -312,16 +313,7 @@ attn_status attn_mqa_logits_fp8(const void* q, const void* kv, const float* kv_s
   p.S_kv = S_kv;
   p.H = H;
   p.clean = clean_logits;
-  // Enough query groups per CTA to amortize loading the key tile, few enough
-  // that short key ranges still give every SM work.
-  const int groups = (S_q + attn_sm103a::mqa_rows_per_group(H) - 1) /
-                     attn_sm103a::mqa_rows_per_group(H);
-  const int64_t key_tiles = (S_kv + attn_sm103a::mqa_keys_per_cta() - 1) /
-                            attn_sm103a::mqa_keys_per_cta();
-  int per = 16;
-  while (per > 1 && key_tiles * ((groups + per - 1) / per) < 2 * st->num_sms) per /= 2;
-  p.groups_per_cta = per;
-  if ((groups + per - 1) / per > 65535) return fail(ATTN_ERR_UNSUPPORTED, "S_q too large");
+  p.tiles_per_cta = attn_sm103a::mqa_tiles_per_cta(S_q, S_kv, H, st->num_sms);
   p.err = st->err_word;
   p.wait_limit_ns = g_wait_limit_ns.load();
   cudaError_t e = attn_sm103a::mqa_logits_launch(mq, mk, p, stream);

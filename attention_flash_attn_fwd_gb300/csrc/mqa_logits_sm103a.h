@@ -17,16 +17,21 @@ struct MqaParams {
   int64_t stride;          // row stride of logits, >= S_kv
   int S_q, S_kv, H;        // H in {32, 64, 128}; D = 128
   int clean;               // 1: -inf outside the window
-  int groups_per_cta;      // query groups each CTA walks
+  int tiles_per_cta;       // 128-key tiles each CTA walks
   int* err;                // device error word
   uint64_t wait_limit_ns;  // bound on every mbarrier wait
 };
 
-// q map: E4M3 [S_q * H, 128] as 2-D, box 128 x 256 rows, 128-byte swizzle;
-// k map: E4M3 [S_kv, 128] as 2-D, box 128 x 128 rows, 128-byte swizzle.
+// q map: E4M3 [S_q * H, 128] as 2-D, box 128 x mqa_rows_per_slab_box() rows;
+// k map: E4M3 [S_kv, 128] as 2-D, box 128 x mqa_keys_per_tile() rows; both
+// with 128-byte swizzle.  The grid is (query blocks of mqa_rows_per_block(H)
+// rows) x (key splits of p.tiles_per_cta tiles).
 cudaError_t mqa_logits_launch(const CUtensorMap& q, const CUtensorMap& k, const MqaParams& p,
                               cudaStream_t stream);
-int mqa_rows_per_group(int H);
-int mqa_keys_per_cta();
+int mqa_rows_per_block(int H);
+int mqa_keys_per_tile();
+int mqa_rows_per_slab_box();
+// Tiles per CTA that balance the grid over num_sms SMs.
+int mqa_tiles_per_cta(int S_q, int S_kv, int H, int num_sms);
 
 }  // namespace attn_sm103a

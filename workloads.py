@@ -212,7 +212,7 @@ class MqaCase:
 
 
 # Long-context indexer shape of the page's sweep (2048 x 131072 is its largest;
-# this one keeps the output at 1 GB): 1024 rows x 65536 keys, 64 heads, D=128.
+# this one keeps the fp32 output at 256 MiB): 1024 rows x 65536 keys, 64 heads, D=128.
 C9 = MqaCase("mqa_logits_fp8_sq1024_skv65536_h64_d128_causal", 1024, 65536, 64, 128, "causal")
 
 # Prefix-cached prefill: 8 requests of 1024 new tokens each on top of cached
