@@ -113,20 +113,40 @@ __device__ __forceinline__ KeyScale key_scale(float scale) {
   return k;
 }
 
-// One 64-column chunk (slab columns kCol0 .. kCol0 + 63) of one 16-lane half
-// of a warp's 32 keys: v holds keys g (v[4r], v[4r+1]) and g + 8 (v[4r+2],
-// v[4r+3]) at columns kCol0 + 8r + 2c and kCol0 + 8r + 2c + 1.  Accumulates
-// w * relu(scale * x) per (row of the slab, key) as packed pairs.
-template <int H, bool kSat, int kCol0>
-__device__ __forceinline__ void accumulate_chunk(const float (&v)[32], const float* w_slab, int c,
-                                                 const KeyScale& k0, const KeyScale& k1,
-                                                 uint64_t (&a)[kCols / H][2]) {
+// For a key scale >= 0, relu(scale * x) = scale * relu(x): the head sum is
+// taken over relu(x) and scaled once.  relu of a float is a signed-integer
+// max with 0 on its bits (negative floats, -0 included, are negative
+// integers), one ALU instruction that leaves the FMA pipe to a packed
+// f32x2 FMA over the column pairs the load already delivers adjacent.
+template <int H>
+__device__ __forceinline__ void accumulate_half_pos(const float (&v)[64], const float* w_slab, int c,
+                                                    uint64_t (&a)[kCols / H][2]) {
 #pragma unroll
-  for (int r = 0; r < 8; ++r) {
-    const int col = kCol0 + 8 * r;
-    const int row = col / H;  // a repetition's 8 columns never straddle rows (H % 8 == 0)
-    const float2 w2 = *reinterpret_cast<const float2*>(&w_slab[col + 2 * c]);
+  for (int r = 0; r < 16; ++r) {
+    const int row = (8 * r) / H;
+    const float2 w2 = *reinterpret_cast<const float2*>(&w_slab[8 * r + 2 * c]);
     const uint64_t wp = f2_pack(w2.x, w2.y);
+    const float y0 = __int_as_float(max(__float_as_int(v[4 * r]), 0));
+    const float y1 = __int_as_float(max(__float_as_int(v[4 * r + 1]), 0));
+    const float y2 = __int_as_float(max(__float_as_int(v[4 * r + 2]), 0));
+    const float y3 = __int_as_float(max(__float_as_int(v[4 * r + 3]), 0));
+    a[row][0] = f2_fma(f2_pack(y0, y1), wp, a[row][0]);
+    a[row][1] = f2_fma(f2_pack(y2, y3), wp, a[row][1]);
+  }
+}
+
+// One 16-lane half of a warp's 32 keys: v holds keys g (v[4r], v[4r+1]) and
+// g + 8 (v[4r+2], v[4r+3]) at slab columns 8r + 2c and 8r + 2c + 1.
+// Accumulates w * relu(scale * x) per (row of the slab, key, column parity)
+// in scalar registers: one saturating multiply and one FMA per element.
+template <int H, bool kSat>
+__device__ __forceinline__ void accumulate_half(const float (&v)[64], const float* w_slab, int c,
+                                                const KeyScale& k0, const KeyScale& k1,
+                                                float (&a)[kCols / H][2][2]) {
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    const int row = (8 * r) / H;  // a repetition's 8 columns never straddle rows (H % 8 == 0)
+    const float2 w2 = *reinterpret_cast<const float2*>(&w_slab[8 * r + 2 * c]);
     float y0, y1, y2, y3;
     if (kSat) {
       y0 = mul_sat(v[4 * r], k0.s_sat);
@@ -139,30 +159,11 @@ __device__ __forceinline__ void accumulate_chunk(const float (&v)[32], const flo
       y2 = fmaxf(v[4 * r + 2] * k1.s_sat, 0.f);
       y3 = fmaxf(v[4 * r + 3] * k1.s_sat, 0.f);
     }
-    a[row][0] = f2_fma(f2_pack(y0, y1), wp, a[row][0]);
-    a[row][1] = f2_fma(f2_pack(y2, y3), wp, a[row][1]);
+    a[row][0][0] = fmaf(y0, w2.x, a[row][0][0]);
+    a[row][0][1] = fmaf(y1, w2.y, a[row][0][1]);
+    a[row][1][0] = fmaf(y2, w2.x, a[row][1][0]);
+    a[row][1][1] = fmaf(y3, w2.y, a[row][1][1]);
   }
-}
-
-// Chunks 0-2 of a unit: chunk 0 is already loading into P.  The chunks go
-// through the one register buffer; a load's latency is covered by the other
-// epilogue warps of the SM sub-partition.  Returns with chunk 3 in P.
-template <int H, bool kSat>
-__device__ __forceinline__ void accumulate_first3(uint32_t taddr, float (&P)[32],
-                                                  const float* w_slab, int c,
-                                                  const KeyScale (&ks)[2][2],
-                                                  uint64_t (&a)[2][kCols / H][2]) {
-  constexpr uint32_t kHalf = 16u << 16;
-  tmem_wait_ld_into(P);
-  accumulate_chunk<H, kSat, 0>(P, w_slab, c, ks[0][0], ks[0][1], a[0]);
-  tmem_ld16x256b_x8(taddr + 64, P);
-  tmem_wait_ld_into(P);
-  accumulate_chunk<H, kSat, 64>(P, w_slab, c, ks[0][0], ks[0][1], a[0]);
-  tmem_ld16x256b_x8(taddr + kHalf, P);
-  tmem_wait_ld_into(P);
-  accumulate_chunk<H, kSat, 0>(P, w_slab, c, ks[1][0], ks[1][1], a[1]);
-  tmem_ld16x256b_x8(taddr + kHalf + 64, P);
-  tmem_wait_ld_into(P);
 }
 
 template <int H>
@@ -173,8 +174,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kRows = kSlabs * R;    // query rows per block (<= 32)
   static_assert(kRows <= 32 && R <= 4, "a block's rows fit one warp's lanes");
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  // Offset from the __shared__ array (not integer arithmetic on its address),
+  // so the compiler keeps every access in the shared state space.
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Stats* stats = reinterpret_cast<Stats*>(smem + kOffStats);
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + kOffCtl);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -346,66 +348,105 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     if (n_t > 0) fetch_scales(0);
     // This warpgroup's units in order: v = wg, wg + 3, ... (tile v / kSlabs,
-    // slab v % kSlabs, buffer v % kBufs).  A unit is read in four 64-column
-    // chunks; chunk 0 of the next unit loads while chunk 3 of this one is
-    // summed.
+    // slab v % kSlabs, buffer v % kBufs).  A unit is read as two 64-register
+    // halves; the latency of each load is covered by the other epilogue warps
+    // of the SM sub-partition.
     const int n_units = n_t * kSlabs;
-    float P[32], Q[32];
-    bool live = false;
-    auto open_unit = [&](int v) -> bool {  // wait for unit v, start loading its chunk 0
-      const int b = v % kBufs;
-      if (!__all_sync(0xffffffffu, mbar_wait_sleep(&ctl->s_full[b], (v / kBufs) & 1, p.wait_limit_ns,
-                                             p.err, 170)))
-        return false;
-      tc_fence_after_sync();
-      live = slab_live(stats->slo[v % kSlabs], stats->shi[v % kSlabs],
-                       (t_begin + v / kSlabs) * kKeys);
-      if (live) tmem_ld16x256b_x8(lane_addr + kCols * b, P);
-      return true;
-    };
-    if (wg < n_units && ok) ok = open_unit(wg);
     KeyScale ks[2][2];
-    bool sat = true;
+    float kraw[2][2];
+    bool sat = true, pos = true;
     int cur_tl = -1;
     for (int v = wg; v < n_units && ok; v += kEpiGroups) {
       const int tl = v / kSlabs, s = v % kSlabs, b = v % kBufs;
       const int key0 = (t_begin + tl) * kKeys;
       if (tl != cur_tl) {  // this warpgroup visits every tile, in order
         cur_tl = tl;
+        pos = true;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
-          for (int kp = 0; kp < 2; ++kp) ks[hf][kp] = key_scale(nraw[hf][kp]);
+          for (int kp = 0; kp < 2; ++kp) {
+            kraw[hf][kp] = nraw[hf][kp];
+            ks[hf][kp] = key_scale(nraw[hf][kp]);
+            pos = pos && nraw[hf][kp] >= 0.f && nraw[hf][kp] <= 3.0e38f;
+          }
         if (tl + 1 < n_t) fetch_scales(tl + 1);
         sat = ks[0][0].by_sat && ks[0][1].by_sat && ks[1][0].by_sat && ks[1][1].by_sat;
+        // The path is chosen per warp, never per thread: the branches hold
+        // warp-collective tensor-memory loads (.sync.aligned), __syncwarp and
+        // the barrier arrive, which the whole warp must reach together.
+        pos = __all_sync(0xffffffffu, pos);
+        sat = __all_sync(0xffffffffu, sat);
       }
-      const bool cur_live = live;
-      uint64_t a[2][R][2];  // [half][row][key of the pair]
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-        for (int r = 0; r < R; ++r) a[hf][r][0] = a[hf][r][1] = f2_pack(0.f, 0.f);
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(&ctl->s_full[b], (v / kBufs) & 1, p.wait_limit_ns, p.err, 170));
+      if (!ok) break;
+      tc_fence_after_sync();
+      const bool live = slab_live(stats->slo[s], stats->shi[s], key0);
+      float u[2][R][2];  // [half][row][key of the pair]: this thread's partial head sums
       const float* w_slab = stats->w + s * kCols;
       const uint32_t taddr = lane_addr + kCols * b;
-      if (cur_live) {
-        if (sat)
-          accumulate_first3<H, true>(taddr, P, w_slab, c, ks, a);
-        else
-          accumulate_first3<H, false>(taddr, P, w_slab, c, ks, a);
+      if (live && pos) {
+        uint64_t a2[2][R][2];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) Q[e] = P[e];
-      }
-      // The whole buffer is in registers (or was never needed): hand it back
-      // and open the next unit before summing the last chunk.
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->t_empty[b]);
-      if (v + kEpiGroups < n_units) ok = open_unit(v + kEpiGroups);
-      if (cur_live) {
+        for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+          for (int r = 0; r < R; ++r) a2[hf][r][0] = a2[hf][r][1] = f2_pack(0.f, 0.f);
+        float x[64];
+        tmem_ld16x256b_x16_wait(taddr, x);
+        accumulate_half_pos<H>(x, w_slab, c, a2[0]);
+        tmem_ld16x256b_x16_wait(taddr + (16u << 16), x);
+        // The whole buffer is in registers: hand it back.
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->t_empty[b]);
+        accumulate_half_pos<H>(x, w_slab, c, a2[1]);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+          for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int kp = 0; kp < 2; ++kp) {
+              float lo, hi;
+              f2_unpack(a2[hf][r][kp], lo, hi);
+              u[hf][r][kp] = lo + hi;
+            }
+      } else if (live) {
+        float a[2][R][2][2];  // [half][row][key of the pair][column parity]
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+          for (int r = 0; r < R; ++r)
+            a[hf][r][0][0] = a[hf][r][0][1] = a[hf][r][1][0] = a[hf][r][1][1] = 0.f;
+        float x[64];
+        tmem_ld16x256b_x16_wait(taddr, x);
         if (sat)
-          accumulate_chunk<H, true, 64>(Q, w_slab, c, ks[1][0], ks[1][1], a[1]);
+          accumulate_half<H, true>(x, w_slab, c, ks[0][0], ks[0][1], a[0]);
         else
-          accumulate_chunk<H, false, 64>(Q, w_slab, c, ks[1][0], ks[1][1], a[1]);
+          accumulate_half<H, false>(x, w_slab, c, ks[0][0], ks[0][1], a[0]);
+        tmem_ld16x256b_x16_wait(taddr + (16u << 16), x);
+        // The whole buffer is in registers: hand it back.
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->t_empty[b]);
+        if (sat)
+          accumulate_half<H, true>(x, w_slab, c, ks[1][0], ks[1][1], a[1]);
+        else
+          accumulate_half<H, false>(x, w_slab, c, ks[1][0], ks[1][1], a[1]);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+          for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int kp = 0; kp < 2; ++kp) u[hf][r][kp] = a[hf][r][kp][0] + a[hf][r][kp][1];
+      } else {
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->t_empty[b]);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+          for (int r = 0; r < R; ++r) u[hf][r][0] = u[hf][r][1] = 0.f;
       }
       // Head sum across the 4 threads sharing a key: first over the key pair
       // (lane bit 0 keeps kp = c & 1), then over the halves (bit 1 keeps
@@ -416,18 +457,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         float y[2];
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
-          float x0l, x0h, x1l, x1h;
-          f2_unpack(a[hf][r][0], x0l, x0h);
-          f2_unpack(a[hf][r][1], x1l, x1h);
-          const float u0 = x0l + x0h, u1 = x1l + x1h;
+          const float u0 = u[hf][r][0], u1 = u[hf][r][1];
           const float keep = (c & 1) ? u1 : u0, send = (c & 1) ? u0 : u1;
           y[hf] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
         }
         const float keep = (c & 2) ? y[1] : y[0], send = (c & 2) ? y[0] : y[1];
         z[r] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
       }
-      const float unscale = (c & 2) ? ((c & 1) ? ks[1][1].unscale : ks[1][0].unscale)
-                                    : ((c & 1) ? ks[0][1].unscale : ks[0][0].unscale);
+      const float unscale =
+          pos ? ((c & 2) ? ((c & 1) ? kraw[1][1] : kraw[1][0]) : ((c & 1) ? kraw[0][1] : kraw[0][0]))
+              : ((c & 2) ? ((c & 1) ? ks[1][1].unscale : ks[1][0].unscale)
+                         : ((c & 1) ? ks[0][1].unscale : ks[0][0].unscale));
       const int j = key0 + j_off;
 #pragma unroll
       for (int r = 0; r < R; ++r) {

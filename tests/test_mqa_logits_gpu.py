@@ -55,6 +55,39 @@ def test_mqa_logits_matches_oracle(S_q, S_kv, H, window, clean):
     _check(got, _ref(inputs, clean), "mqa %s" % (case,))
 
 
+@pytest.mark.parametrize("H", [32, 64, 128])
+def test_mqa_logits_special_key_scales(H):
+    """Negative, zero and very large (beyond 2^100) per-key scales: every
+    scale sign and size the kernel's arithmetic distinguishes, mixed within
+    the keys one thread handles."""
+    case = workloads.MqaCase("t", 61, 300, H, 128, "misaligned", True, seed=103)
+    q8, kv8, sc, w, st, en = workloads.make_mqa(case)
+    sc = sc.clone()
+    sc[0::7] = -sc[0::7]
+    sc[3::11] = 0.0
+    sc[5::13] = sc[5::13] * 2.0 ** 110
+    sc[6::17] = -sc[6::17] * 2.0 ** 110
+    out = torch.full((case.S_q, case.S_kv), SENTINEL, device="cuda", dtype=torch.float32)
+    attn.mqa_logits_fp8(q8.cuda(), kv8.cuda(), sc.cuda(), w.cuda(), st.cuda(), en.cuda(),
+                        clean_logits=True, out=out)
+    torch.cuda.synchronize()
+    assert attn.attn_device_error() == 0
+    got = out.cpu().double().numpy()
+    ref = _ref((q8, kv8, sc, w, st, en), True)
+    # Per-key relative check: the huge scales would swamp a global norm.
+    fin = np.isfinite(ref)
+    assert np.array_equal(np.isneginf(got), np.isneginf(ref))
+    for j in range(case.S_kv):
+        col = fin[:, j]
+        if not col.any():
+            continue
+        r, g = ref[col, j], got[col, j]
+        scale = max(np.sqrt(np.mean(r ** 2)), 1e-30)
+        assert np.all(np.isfinite(g)), "key %d" % j
+        assert np.abs(g - r).max() <= MQA_MAX_ABS_REL_RMS * scale or np.all(r == 0) and np.all(
+            g == 0), "key %d: max_abs=%.3e rms=%.3e" % (j, np.abs(g - r).max(), scale)
+
+
 def test_mqa_logits_strided_output_and_determinism():
     """A row stride wider than S_kv leaves the padding untouched; two runs
     give the same bits."""
