@@ -228,7 +228,8 @@ ATTN_API attn_status attn_extend_fwd(const void* q, const void* k_pool, const vo
  *   H_q % H_kv == 0, H_q / H_kv <= 16, D == 128 (else ATTN_ERR_UNSUPPORTED).
  * The library owns a split-partials workspace per (device, stream), grown on
  * demand outside stream capture; growing it during capture returns
- * ATTN_ERR_NO_MEMORY (call once with the largest shapes before capturing).
+ * ATTN_ERR_NO_MEMORY (call once with the largest shapes, on the stream that
+ * will be captured, before capturing).
  * Calls on different streams may run concurrently; calls on one stream use
  * its workspace in stream order.
  */
