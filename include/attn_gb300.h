@@ -225,7 +225,7 @@ ATTN_API attn_status attn_extend_fwd(const void* q, const void* k_pool, const vo
  *              device; > 0: every sequence is split into that many parts.
  *   scale      softmax scale, finite and > 0.
  *   dtype      ATTN_F16 or ATTN_BF16 (ADDED: not in the published signature).
- *   H_q % H_kv == 0, H_q / H_kv <= 16, D == 128 (else ATTN_ERR_UNSUPPORTED).
+ *   H_q % H_kv == 0, H_q / H_kv <= 16, D 64 or 128 (else ATTN_ERR_UNSUPPORTED).
  * The library owns a split-partials workspace per (device, stream), grown on
  * demand outside stream capture; growing it during capture returns
  * ATTN_ERR_NO_MEMORY (call once with the largest shapes, on the stream that
