@@ -59,7 +59,36 @@ struct DeviceState {
     size_t bytes = 0;
   };
   std::unordered_map<cudaStream_t, Workspace> workspaces;
+  // Prefill unit counters (one int per stream): persistent CTAs take their
+  // next query block from it; the host zeroes it before every launch.
+  std::unordered_map<cudaStream_t, int*> sched;
 };
+
+// The stream's prefill unit counter, created on first use outside stream
+// capture.  nullptr (one CTA per unit instead) while a stream without one is
+// being captured.
+attn_status prefill_sched(DeviceState* st, cudaStream_t stream, int** out) {
+  *out = nullptr;
+  std::lock_guard<std::mutex> lk(st->mu);
+  auto it = st->sched.find(stream);
+  if (it == st->sched.end()) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaStreamIsCapturing");
+    if (cs != cudaStreamCaptureStatusNone) return ATTN_OK;
+    int* c = nullptr;
+    e = cudaMalloc(&c, 16);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(ATTN_ERR_NO_MEMORY, std::string("scheduler cudaMalloc: ") + cudaGetErrorString(e));
+    }
+    it = st->sched.emplace(stream, c).first;
+  }
+  cudaError_t e = cudaMemsetAsync(it->second, 0, sizeof(int), stream);
+  if (e != cudaSuccess) return fail_cuda(e, "scheduler reset");
+  *out = it->second;
+  return ATTN_OK;
+}
 
 DeviceState g_dev[kMaxDevices];
 
@@ -257,6 +286,11 @@ attn_status attn_prefill_fwd(const void* q, const void* k, const void* v, void* 
   p.scale_log2 = scale * 1.4426950408889634f;
   p.err = st->err_word;
   p.wait_limit_ns = g_wait_limit_ns.load();
+  p.o = o;
+  p.o_align32 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0 ? 1 : 0;
+  p.ctas = st->num_sms;
+  s = prefill_sched(st, stream, &p.sched);
+  if (s != ATTN_OK) return s;
   cudaError_t e = attn_sm103a::prefill_launch(mq, mk, mv, mo, p, D, bf16, stream);
   if (e != cudaSuccess) return fail_cuda(e, "prefill launch");
   return ATTN_OK;
@@ -448,6 +482,11 @@ attn_status attn_prefill_fp8_fwd(const void* q, const void* k, const void* v, vo
                                     1.4426950408889634);
   p.err = st->err_word;
   p.wait_limit_ns = g_wait_limit_ns.load();
+  p.o = o;
+  p.o_align32 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0 ? 1 : 0;
+  p.ctas = st->num_sms;
+  s = prefill_sched(st, stream, &p.sched);
+  if (s != ATTN_OK) return s;
   cudaError_t e =
       attn_sm103a::prefill_fp8_launch(mq, mk, mv, mo, p, out_dtype == ATTN_BF16, stream);
   if (e != cudaSuccess) return fail_cuda(e, "FP8 prefill launch");
@@ -674,6 +713,12 @@ attn_status attn_release_workspace(void) {
     if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceSynchronize");
     for (auto& kv : st->workspaces) cudaFree(kv.second.ptr);
     st->workspaces.clear();
+  }
+  if (!st->sched.empty()) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceSynchronize");
+    for (auto& kv : st->sched) cudaFree(kv.second);
+    st->sched.clear();
   }
   return ATTN_OK;
 }

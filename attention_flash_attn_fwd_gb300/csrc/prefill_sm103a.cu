@@ -24,7 +24,17 @@
 //    2^8 (the exact result is unchanged: O and l always share one reference);
 //  * causal tiles wholly above the diagonal are never loaded or multiplied
 //    (tile skipping, aiter PR 7412, Changes/Kernel "tile_skip"), only the
-//    diagonal tiles are masked element by element.
+//    diagonal tiles are masked element by element;
+//  * contiguous forms run persistent CTAs (one per SM) that take (batch,
+//    head, query block) units from a per-stream counter in launch order, so
+//    the units in flight are consecutive (their heads' K/V stay in L2) and
+//    faster CTAs take more of the unequal causal units.  Between units nothing
+//    drains: Q_t is refilled once the unit's last S MMA of tile t has read it,
+//    K/V keep streaming through the same ring, the next unit's first S MMAs
+//    run during the epilogue, and O leaves in whole-sector stores straight
+//    from registers (Q's tiles already hold the next unit).  Measured on
+//    GB300, the one-unit CTAs spent ~5.8 us per unit outside the main loop
+//    (set-up, the first Q/K tiles arriving, epilogue, CTA turnover).
 //
 // Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D),
 // O1 [256+D, 256+2D).  P_t (16-bit pairs) overwrites the first 64 columns of
@@ -64,14 +74,17 @@ constexpr int kThreads = 384; // 2 softmax warpgroups + 1 warpgroup {TMA, MMA, 2
 constexpr int kWarpTma = 8;
 constexpr int kWarpMma = 9;
 // Registers are granted per warpgroup: 384 threads launch with 168 each
-// (64512 in all).  The softmax warpgroups take 224, the TMA/MMA warpgroup
-// keeps 56: 2*128*224 + 128*56 = 64512, exactly the launch total.
+// (64512 in all).  The softmax warpgroups take 216, the TMA/MMA warpgroup
+// keeps 72 (its unit loop spills below that): 2*128*216 + 128*72 = 64512,
+// exactly the launch total.
 constexpr int kRegsAtLaunch = 168;
-constexpr int kRegsSoftmax = 224;
-constexpr int kRegsControl = 56;
+constexpr int kRegsSoftmax = 216;
+constexpr int kRegsControl = 72;
 static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsControl <= kThreads * kRegsAtLaunch,
               "register split exceeds the block's launch allocation");
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+constexpr int kCtlBytesFwd = 512;  // reserved for SharedCtl (checked below)
 
 template <int D, bool kFp8 = false>
 struct Cfg {
@@ -85,7 +98,7 @@ struct Cfg {
   // FP8: O has its own staging tiles (a Q tile is too small to hold it).
   static constexpr int kOStageOff = kTiles * kTileBytes + kStages * kTileBytes;
   static constexpr int kSmemData = kOStageOff + (kFp8 ? kTiles * kOTileBytes : 0);
-  static constexpr int kSmemBytes = kSmemData + 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr int kSmemBytes = kSmemData + 1024 /*align*/ + kCtlBytesFwd;
   // tensor-memory columns of S_t and O_t
   __device__ static constexpr uint32_t col_s(int t) { return t * 128u; }
   __device__ static constexpr uint32_t col_o(int t) { return 256u + t * D; }
@@ -93,17 +106,22 @@ struct Cfg {
 
 struct SharedCtl {
   uint64_t q_full[kTiles];
+  uint64_t q_empty[kTiles];    // the unit's last S MMA of tile t has read Q_t
   uint64_t s_full[kTiles];
   uint64_t p_half[kTiles][2];  // P_t keys [0,64) and [64,128) in tensor memory
-  uint64_t o_full;
+  uint64_t o_full[kTiles];     // the unit's last PV MMA of tile t is done
+  uint64_t o_free[kTiles];     // the softmax warps of tile t hold O_t in registers
+  uint64_t unit_full[2];       // a unit id was published in unit_ring
+  uint64_t unit_empty[2];      // the MMA warp and every softmax warp read it
   uint64_t tmem_free;  // every softmax warp is done reading tensor memory
   uint64_t kv_full[10];
   uint64_t kv_empty[10];
   uint64_t tail_v;     // extend form: the V tile holding the sequence end has landed
+  int unit_ring[2];
   uint32_t tmem_base;
   int abort;
 };
-static_assert(sizeof(SharedCtl) <= 256, "control block must fit its reserved bytes");
+static_assert(sizeof(SharedCtl) <= kCtlBytesFwd, "control block must fit its reserved bytes");
 
 // TMA load of one 64-column box of rows [row, row + 128) of (batch b, head h).
 // BHSD maps are (D, S, H, B); BSHD maps are (D, H, S, B).
@@ -275,8 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tm_o, const PrefillParams p) {
   using C = Cfg<D, kFp8>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  // Offset from the __shared__ array, so accesses stay in the shared space.
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* s_q = smem;                                   // kTiles tiles
   uint8_t* s_kv = smem + kTiles * C::kTileBytes;         // kStages tiles
   SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + C::kSmemData);
@@ -284,23 +302,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
 
-  // Work item: (batch, head, 256-row query block); the longest causal blocks
-  // of a (batch, head) are handed out first, heads stay adjacent for L2 reuse.
+  // Work unit: (batch, head, 256-row query block), numbered head-major with
+  // the longest causal block of a head first.  Without a scheduler counter a
+  // CTA runs the one unit its index names; with one (p.sched, contiguous
+  // form) a persistent CTA takes the next unit from it until none is left,
+  // so the CTAs in flight always hold consecutive units: a few heads, whose
+  // K/V stay in L2.
   const int nqb = p.num_q_blocks;
   // A CTA pair (cluster of 2, extend form only) holds query heads 2k, 2k+1.
   const int cs = (kPaged && p.pair) ? 2 : 1;
   const int rank = cs == 2 ? static_cast<int>(cluster_ctarank()) : 0;
-  const int unit = blockIdx.x / cs;
-  const int bh = unit / nqb;
-  const int qb = nqb - 1 - (unit % nqb);
-  const int b = bh / (p.H / cs);
-  const int h = (bh % (p.H / cs)) * cs + rank;
-  const int S_kv = kPaged ? extend_kv_len(b, p) : p.S_kv;  // keys of this sequence
-  const int row_base = qb * (kTiles * kBM);
-  const int n_kv0 = kv_tiles_for(row_base, S_kv, p);
-  const int n_kv1 = kv_tiles_for(row_base + kBM, S_kv, p);
-  auto n_kv = [&](int t) { return t == 0 ? n_kv0 : n_kv1; };  // KV tiles of query tile t
-  const int n_all = max(n_kv0, n_kv1);  // tile 1 never needs fewer than tile 0
+  const int n_units = p.B * (p.H / cs) * nqb;
+  const bool dyn = !kPaged && p.sched != nullptr;
+  struct Unit {
+    int b, h, S_kv, row_base, n_kv0, n_kv1, n_all;
+    __device__ int n_kv(int t) const { return t == 0 ? n_kv0 : n_kv1; }
+  };
+  auto unit_info = [&](int u) {
+    Unit U;
+    const int bh = u / nqb;
+    const int qb = nqb - 1 - (u % nqb);
+    U.b = bh / (p.H / cs);
+    U.h = (bh % (p.H / cs)) * cs + rank;
+    U.S_kv = kPaged ? extend_kv_len(U.b, p) : p.S_kv;  // keys of this sequence
+    U.row_base = qb * (kTiles * kBM);
+    U.n_kv0 = kv_tiles_for(U.row_base, U.S_kv, p);
+    U.n_kv1 = kv_tiles_for(U.row_base + kBM, U.S_kv, p);
+    U.n_all = max(U.n_kv0, U.n_kv1);  // tile 1 never needs fewer than tile 0
+    return U;
+  };
+  // Unit n of this CTA, published by the producer in unit_ring[n % 2]; -1 ends.
+  auto read_unit = [&](int n) -> int {
+    return *reinterpret_cast<volatile int*>(&ctl->unit_ring[n & 1]);
+  };
 
   if (warp == kWarpMma) {
     tmem_alloc(&ctl->tmem_base, 512);
@@ -309,11 +343,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int t = 0; t < kTiles; ++t) {
       mbar_init(&ctl->q_full[t], 1);
+      mbar_init(&ctl->q_empty[t], 1);
       mbar_init(&ctl->s_full[t], 1);
       mbar_init(&ctl->p_half[t][0], 4);
       mbar_init(&ctl->p_half[t][1], 4);
+      mbar_init(&ctl->o_full[t], 1);
+      mbar_init(&ctl->o_free[t], 4);
     }
-    mbar_init(&ctl->o_full, 1);
+    for (int sl = 0; sl < 2; ++sl) {
+      mbar_init(&ctl->unit_full[sl], 1);
+      mbar_init(&ctl->unit_empty[sl], 1 + 8);  // the MMA warp and the 8 softmax warps
+    }
     mbar_init(&ctl->tmem_free, 8);
     mbar_init(&ctl->tail_v, 1);
     for (int s = 0; s < C::kStages; ++s) {
@@ -328,70 +368,114 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (cs == 2) cluster_sync();  // the partner's barriers exist before any multicast
   tc_fence_after_sync();
   const uint32_t tmem = ctl->tmem_base;
+  volatile int* abort_flag = &ctl->abort;
 
   if (warp >= 8) {
    // ============================================= control warpgroup
    setmaxnreg_dec<kRegsControl>();
    if (kPaged && warp == kWarpTma) {
     // ------------------------------------------------- producer (paged K/V)
-    if (n_all > 0) produce_paged<D>(tm_q, tm_k, tm_v, p, ctl, s_q, s_kv, b, h, S_kv, row_base,
-                                    n_all, lane, cs, rank);
+    // One unit per CTA: publish it, stream it, then publish the end.
+    const int u = static_cast<int>(blockIdx.x) / cs;
+    if (lane == 0) {
+      ctl->unit_ring[0] = u;
+      mbar_arrive(&ctl->unit_full[0]);
+    }
+    // Q is loaded even when the unit has no key (the MMA warp waits for it).
+    const Unit U = unit_info(u);
+    produce_paged<D>(tm_q, tm_k, tm_v, p, ctl, s_q, s_kv, U.b, U.h, U.S_kv, U.row_base, U.n_all,
+                     lane, cs, rank);
+    if (lane == 0) {
+      ctl->unit_ring[1] = -1;
+      mbar_arrive(&ctl->unit_full[1]);
+    }
     __syncwarp();
    } else if (warp == kWarpTma) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n_all > 0) {
-      int issued = 0;  // KV loads issued so far
+    if (lane == 0) {
       tma_prefetch_map(&tm_q);
       tma_prefetch_map(&tm_k);
       tma_prefetch_map(&tm_v);
-      for (int t = 0; t < kTiles; ++t) {
+      int issued = 0;    // K/V loads issued, all units
+      int q_loads = 0;   // units whose Q was loaded
+      bool ok = true;
+      auto load_q = [&](const Unit& U, int n, int t) {
+        if (n > 0 && !(ok = mbar_wait(&ctl->q_empty[t], (n - 1) & 1, p.wait_limit_ns, p.err, 16)))
+          return;
         mbar_arrive_expect_tx(&ctl->q_full[t], C::kTileBytes);
         for (int x = 0; x < C::kBoxes; ++x)
           load_box(s_q + t * C::kTileBytes + x * (kBM * 128), &tm_q, &ctl->q_full[t],
-                   x * C::kBoxCols, row_base + t * kBM, h, b, p.bshd);
-      }
-      for (int j = 0; j < min(n_all, kL2PrefetchTiles); ++j)
-        for (int x = 0; x < C::kBoxes; ++x) {
-          prefetch_box(&tm_k, x * C::kBoxCols, j * kBN, h, b, p.bshd);
-          prefetch_box(&tm_v, x * C::kBoxCols, j * kBN, h, b, p.bshd);
-        }
-      volatile int* abort_flag = &ctl->abort;
-      for (int j = 0; j < n_all && !*abort_flag; ++j) {
-        if (j + kL2PrefetchTiles < n_all)
-          for (int x = 0; x < C::kBoxes; ++x) {
-            prefetch_box(&tm_k, x * C::kBoxCols, (j + kL2PrefetchTiles) * kBN, h, b, p.bshd);
-            prefetch_box(&tm_v, x * C::kBoxCols, (j + kL2PrefetchTiles) * kBN, h, b, p.bshd);
-          }
+                   x * C::kBoxCols, U.row_base + t * kBM, U.h, U.b, p.bshd);
+      };
+      auto load_kv = [&](const Unit& U, int j) {
 #pragma unroll
         for (int kind = 0; kind < 2; ++kind) {
-          const int idx = 2 * j + kind;
-          const int st = idx % C::kStages;
-          const int round = idx / C::kStages;
+          const int st = issued % C::kStages;
+          const int round = issued / C::kStages;
           if (round > 0 &&
-              !mbar_wait(&ctl->kv_empty[st], (round - 1) & 1, p.wait_limit_ns, p.err, 10)) {
-            *abort_flag = 1;
-            break;
-          }
+              !(ok = mbar_wait(&ctl->kv_empty[st], (round - 1) & 1, p.wait_limit_ns, p.err, 10)))
+            return;
           uint8_t* dst = s_kv + st * C::kTileBytes;
           mbar_arrive_expect_tx(&ctl->kv_full[st], C::kTileBytes);
           const CUtensorMap* map = kind == 0 ? &tm_k : &tm_v;
           for (int x = 0; x < C::kBoxes; ++x)
-            load_box(dst + x * (kBN * 128), map, &ctl->kv_full[st], x * C::kBoxCols, j * kBN,
-                     h, b, p.bshd);
-          issued = idx + 1;
+            load_box(dst + x * (kBN * 128), map, &ctl->kv_full[st], x * C::kBoxCols, j * kBN, U.h,
+                     U.b, p.bshd);
+          ++issued;
+        }
+      };
+      // A unit is taken only when the previous one is fully issued, so
+      // faster CTAs take more of the (unequal, causal) units.
+      for (int n = 0; ok; ++n) {
+        int u = dyn ? atomicAdd(p.sched, 1) : (n == 0 ? static_cast<int>(blockIdx.x) : n_units);
+        if (u >= n_units || *abort_flag) u = -1;
+        const int slot = n & 1;
+        if (n >= 2 &&
+            !(ok = mbar_wait(&ctl->unit_empty[slot], ((n >> 1) - 1) & 1, p.wait_limit_ns, p.err,
+                             17)))
+          break;
+        ctl->unit_ring[slot] = u;
+        mbar_arrive(&ctl->unit_full[slot]);  // release: the id is visible to the waiters
+        if (u < 0) break;
+        const Unit U = unit_info(u);
+        for (int j = 0; j < min(U.n_all, kL2PrefetchTiles); ++j)
+          for (int x = 0; x < C::kBoxes; ++x) {
+            prefetch_box(&tm_k, x * C::kBoxCols, j * kBN, U.h, U.b, p.bshd);
+            prefetch_box(&tm_v, x * C::kBoxCols, j * kBN, U.h, U.b, p.bshd);
+          }
+        // Q_0, the first K/V tile, then Q_1: each Q tile is refilled as soon
+        // as the previous unit's last S MMA of that tile has read it, and the
+        // first K/V tile does not wait for the later Q tile.
+        load_q(U, n, 0);
+        if (ok && U.n_all > 0) load_kv(U, 0);
+        if (ok) load_q(U, n, 1);
+        if (!ok) break;
+        q_loads = n + 1;
+        for (int j = 1; j < U.n_all && ok && !*abort_flag; ++j) {
+          if (j - 1 + kL2PrefetchTiles < U.n_all)
+            for (int x = 0; x < C::kBoxes; ++x) {
+              prefetch_box(&tm_k, x * C::kBoxCols, (j - 1 + kL2PrefetchTiles) * kBN, U.h, U.b,
+                           p.bshd);
+              prefetch_box(&tm_v, x * C::kBoxCols, (j - 1 + kL2PrefetchTiles) * kBN, U.h, U.b,
+                           p.bshd);
+            }
+          load_kv(U, j);
         }
       }
+      if (!ok) *abort_flag = 1;
       // Never leave the CTA with a copy still landing in shared memory: wait
       // (bounded) for the last load issued into every stage and for Q.
       for (int idx = max(0, issued - C::kStages); idx < issued; ++idx)
         mbar_wait(&ctl->kv_full[idx % C::kStages], (idx / C::kStages) & 1, p.wait_limit_ns,
                   p.err, 11);
-      for (int t = 0; t < kTiles; ++t) mbar_wait(&ctl->q_full[t], 0, p.wait_limit_ns, p.err, 12);
+      if (q_loads > 0)
+        for (int t = 0; t < kTiles; ++t)
+          mbar_wait(&ctl->q_full[t], (q_loads - 1) & 1, p.wait_limit_ns, p.err, 12);
     }
     __syncwarp();
    } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_all > 0) {
+    if (lane == 0) {
       constexpr uint32_t id_s =
           kFp8 ? idesc_e4m3(kBM, kBN, false, false) : idesc_f16(kBF16, kBM, kBN, false, false);
       constexpr uint32_t id_o =
@@ -399,8 +483,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t q_addr = smem_u32(s_q);
       const uint32_t kv_addr = smem_u32(s_kv);
       bool ok = true;
-      for (int t = 0; t < kTiles && ok; ++t)
-        ok = mbar_wait(&ctl->q_full[t], 0, p.wait_limit_ns, p.err, 20);
 
       // Descriptors are built once; inside the loops each MMA only adds a
       // compile-time offset to a low word, so the issuing thread can feed
@@ -450,53 +532,77 @@ __global__ void __launch_bounds__(kThreads, 1)
                          p.wait_limit_ns, p.err, site);
       };
 
-      if (ok && (ok = wait_full(0, 21))) {
-        tc_fence_after_sync();
-        for (int t = 0; t < kTiles; ++t)
-          if (n_kv(t) > 0) {
-            issue_s(t, 0);
+      int base = 0;         // K/V stages consumed by earlier units
+      int np[kTiles] = {};  // P tiles consumed per query tile, all units
+      for (int n = 0; ok; ++n) {
+        if (!(ok = mbar_wait(&ctl->unit_full[n & 1], (n >> 1) & 1, p.wait_limit_ns, p.err, 28)))
+          break;
+        const int u = read_unit(n);
+        mbar_arrive(&ctl->unit_empty[n & 1]);
+        if (u < 0) break;
+        const Unit U = unit_info(u);
+        // Each query tile releases its Q (q_empty) after its last S MMA and
+        // signals its O (o_full) after its last PV MMA, exactly once per unit.
+        if (U.n_all > 0 && !(ok = wait_full(base, 21))) break;
+        for (int t = 0; t < kTiles && ok; ++t) {
+          if (!(ok = mbar_wait(&ctl->q_full[t], n & 1, p.wait_limit_ns, p.err, 20))) break;
+          tc_fence_after_sync();
+          if (U.n_kv(t) > 0) {
+            issue_s(t, base % C::kStages);
             mma_commit(&ctl->s_full[t]);
           }
-        release(0);
-      }
-      for (int j = 0; j < n_all && ok; ++j) {
-        const int st_v = (2 * j + 1) % C::kStages;
-        const int st_kn = (2 * j + 2) % C::kStages;
-        const bool next = j + 1 < n_all;
-        bool kn_ready = false;
-        if (!(ok = wait_full(2 * j + 1, 22))) break;
-        for (int t = 0; t < kTiles && ok; ++t) {
-          if (j < n_kv(t)) {
-            for (int hf = 0; hf < 2 && ok; ++hf) {
-              ok = mbar_wait(&ctl->p_half[t][hf], j & 1, p.wait_limit_ns, p.err, 23 + 2 * t + hf);
+          if (U.n_kv(t) <= 1) mma_commit(&ctl->q_empty[t]);
+          if (U.n_kv(t) == 0) mma_commit(&ctl->o_full[t]);
+        }
+        if (!ok) break;
+        if (U.n_all > 0) release(base % C::kStages);
+        for (int j = 0; j < U.n_all && ok; ++j) {
+          const int st_v = (base + 2 * j + 1) % C::kStages;
+          const int st_kn = (base + 2 * j + 2) % C::kStages;
+          const bool next = j + 1 < U.n_all;
+          bool kn_ready = false;
+          if (!(ok = wait_full(base + 2 * j + 1, 22))) break;
+          for (int t = 0; t < kTiles && ok; ++t) {
+            if (j < U.n_kv(t)) {
+              // The first PV of a unit overwrites O_t: the previous unit's
+              // epilogue must hold it in registers by then.
+              if (j == 0 && n > 0 &&
+                  !(ok = mbar_wait(&ctl->o_free[t], (n - 1) & 1, p.wait_limit_ns, p.err, 29)))
+                break;
+              for (int hf = 0; hf < 2 && ok; ++hf) {
+                ok = mbar_wait(&ctl->p_half[t][hf], np[t] & 1, p.wait_limit_ns, p.err,
+                               23 + 2 * t + hf);
+                if (!ok) break;
+                tc_fence_after_sync();
+                issue_pv_half(t, st_v, j > 0, hf);
+              }
               if (!ok) break;
-              tc_fence_after_sync();
-              issue_pv_half(t, st_v, j > 0, hf);
+              ++np[t];
+              if (j == U.n_kv(t) - 1) mma_commit(&ctl->o_full[t]);
             }
-            if (!ok) break;
-          }
-          if (t == kTiles - 1) release(st_v);
-          if (next) {
-            if (!kn_ready) {
-              if (!(ok = wait_full(2 * j + 2, 25))) break;
-              kn_ready = true;
-              tc_fence_after_sync();
+            if (t == kTiles - 1) release(st_v);
+            if (next) {
+              if (!kn_ready) {
+                if (!(ok = wait_full(base + 2 * j + 2, 25))) break;
+                kn_ready = true;
+                tc_fence_after_sync();
+              }
+              if (j + 1 < U.n_kv(t)) {
+                issue_s(t, st_kn);
+                mma_commit(&ctl->s_full[t]);
+                if (j + 1 == U.n_kv(t) - 1) mma_commit(&ctl->q_empty[t]);
+              }
+              if (t == kTiles - 1) release(st_kn);
             }
-            if (j + 1 < n_kv(t)) {
-              issue_s(t, st_kn);
-              mma_commit(&ctl->s_full[t]);
-            }
-            if (t == kTiles - 1) release(st_kn);
           }
         }
+        base += 2 * U.n_all;
       }
-      mma_commit(&ctl->o_full);
-      if (!ok) *reinterpret_cast<volatile int*>(&ctl->abort) = 1;
-      // No MMA may still be running when tensor memory is released.
-      mbar_wait(&ctl->o_full, 0, p.wait_limit_ns, p.err, 26);
+      if (!ok) *abort_flag = 1;
     }
     __syncwarp();
-    // Release tensor memory once every softmax warp has read its last O.
+    // Release tensor memory once every softmax warp has read its last O
+    // (which follows every MMA of this CTA).
     mbar_wait(&ctl->tmem_free, 0, p.wait_limit_ns, p.err, 27);
     tc_fence_after_sync();
     tmem_dealloc(tmem, 512);
@@ -507,162 +613,228 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = warp / 4;             // query tile of this warpgroup
     const int wl = warp % 4;            // warp's TMEM lane quarter
     const int r = wl * 32 + lane;       // row within the tile
-    const int row0 = row_base + t * kBM;
-    const int i = row0 + r;             // query index
-    const int diag = S_kv - p.S_q;      // bottom-right causal offset
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wl * 32) << 16);
     const uint32_t col_s = C::col_s(t);
     const uint32_t col_o = C::col_o(t);
     const float c = p.scale_log2;
-
-    float m2 = -INFINITY;  // running reference max, scaled log2 units
-    float l = 0.f;         // running sum of exponentials relative to m2
+    int ns = 0;  // S tiles of this query tile consumed, all units
     bool ok = true;
-    for (int j = 0; j < n_kv(t); ++j) {
+    for (int n = 0; ok; ++n) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&ctl->unit_full[n & 1], (n >> 1) & 1,
+                                             p.wait_limit_ns, p.err, 42));
+      if (!ok) break;
+      const int u = read_unit(n);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->unit_empty[n & 1]);
+      if (u < 0) break;
+      // Only what this tile needs of the unit stays live through the loop.
+      int b, h, S_kv, row0, n_kv;
+      {
+        const Unit U = unit_info(u);
+        b = U.b;
+        h = U.h;
+        S_kv = U.S_kv;
+        row0 = U.row_base + t * kBM;
+        n_kv = U.n_kv(t);
+      }
+      const int i = row0 + r;             // query index
+      const int diag = S_kv - p.S_q;      // bottom-right causal offset
+
+      float m2 = -INFINITY;  // running reference max, scaled log2 units
+      float l = 0.f;         // running sum of exponentials relative to m2
+      for (int j = 0; j < n_kv; ++j, ++ns) {
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(&ctl->s_full[t], ns & 1, p.wait_limit_ns, p.err, 30 + t));
+        if (!ok) break;
+        tc_fence_after_sync();
+        float s[kBN];
+        tmem_ld128_wait(lane_addr + col_s, s);
+        const int key0 = j * kBN;
+        const bool full = (key0 + kBN <= S_kv) && (!p.causal || key0 + kBN - 1 <= row0 + diag);
+        if (!full) {
+          const int lim = p.causal ? min(S_kv - 1, i + diag) : S_kv - 1;
+#pragma unroll
+          for (int cc = 0; cc < kBN; ++cc)
+            if (key0 + cc > lim) s[cc] = -INFINITY;
+        }
+        // Row max: eight independent chains of 3-input max, then a short tree.
+        float mx[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) mx[q] = fmax3(s[3 * q], s[3 * q + 1], s[3 * q + 2]);  // 0..23
+#pragma unroll
+        for (int cc = 24; cc < kBN - 8; cc += 16)
+#pragma unroll
+          for (int q = 0; q < 8; ++q) mx[q] = fmax3(mx[q], s[cc + 2 * q], s[cc + 2 * q + 1]);
+        // columns 24 .. 119 consumed; 120 .. 127 remain
+#pragma unroll
+        for (int q = 0; q < 8; ++q) mx[q] = fmaxf(mx[q], s[kBN - 8 + q]);
+        const float m_raw = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                                  fmaxf(mx[6], mx[7]));
+        const float m_new = fmaxf(m2, m_raw * c);
+        float alpha = 1.f;
+        bool need = false;
+        if (m_new > m2 + kRescaleThreshold) {  // false while m_new == -inf
+          alpha = ex2_approx(m2 - m_new);      // 0 on the first visible tile
+          need = (j > 0);
+          m2 = m_new;
+        }
+        if (__any_sync(0xffffffffu, need)) {
+          // O_t row *= alpha before any of P_t,j is published.  PV_t,j-1
+          // completed before S_t,j was signalled.
+#pragma unroll 1
+          for (int cc = 0; cc < D; cc += 32) {
+            uint32_t o[32];
+            tmem_ld32_wait(lane_addr + col_o + cc, o);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * alpha);
+            tmem_st32(lane_addr + col_o + cc, o);
+          }
+        }
+        const float mref = (m2 == -INFINITY) ? 0.f : m2;
+        const uint64_t c2 = f2_pack(c, c);
+        const uint64_t nm2 = f2_pack(-mref, -mref);
+        uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          if constexpr (kFp8) {
+            uint32_t pk[16];  // 64 keys as E4M3, four per column
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+              float x0, x1, x2, x3;
+              f2_unpack(f2_fma(f2_pack(s[half * 64 + 4 * q], s[half * 64 + 4 * q + 1]), c2, nm2),
+                        x0, x1);
+              f2_unpack(f2_fma(f2_pack(s[half * 64 + 4 * q + 2], s[half * 64 + 4 * q + 3]), c2,
+                               nm2),
+                        x2, x3);
+              const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
+              const float e2 = ex2_approx(x2), e3 = ex2_approx(x3);
+              acc0 = f2_add(acc0, f2_pack(e0, e1));
+              acc1 = f2_add(acc1, f2_pack(e2, e3));
+              pk[q] = pack4_e4m3(e0, e1, e2, e3);
+            }
+            tmem_st16(lane_addr + col_s + half * 16, pk);
+          } else {
+            uint32_t pk[32];
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+              float x0, x1;
+              f2_unpack(f2_fma(f2_pack(s[half * 64 + 2 * q], s[half * 64 + 2 * q + 1]), c2, nm2),
+                        x0, x1);
+              const float e0 = ex2_approx(x0);
+              const float e1 = ex2_approx(x1);
+              if (q & 1)
+                acc1 = f2_add(acc1, f2_pack(e0, e1));
+              else
+                acc0 = f2_add(acc0, f2_pack(e0, e1));
+              pk[q] = pack2<kBF16>(e0, e1);
+            }
+            tmem_st32(lane_addr + col_s + half * 32, pk);
+          }
+          tmem_st_wait();
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl->p_half[t][half]);
+        }
+        float a0, a1, b0, b1;
+        f2_unpack(acc0, a0, a1);
+        f2_unpack(acc1, b0, b1);
+        l = l * alpha + ((a0 + a1) + (b0 + b1));
+      }
+      if (!ok) break;
+
+      // ---------------------------------------------------------- epilogue
       ok = __all_sync(0xffffffffu,
-                      mbar_wait(&ctl->s_full[t], j & 1, p.wait_limit_ns, p.err, 30 + t));
+                      mbar_wait(&ctl->o_full[t], n & 1, p.wait_limit_ns, p.err, 40 + t));
       if (!ok) break;
       tc_fence_after_sync();
-      float s[kBN];
-      tmem_ld128_wait(lane_addr + col_s, s);
-      const int key0 = j * kBN;
-      const bool full = (key0 + kBN <= S_kv) && (!p.causal || key0 + kBN - 1 <= row0 + diag);
-      if (!full) {
-        const int lim = p.causal ? min(S_kv - 1, i + diag) : S_kv - 1;
-#pragma unroll
-        for (int cc = 0; cc < kBN; ++cc)
-          if (key0 + cc > lim) s[cc] = -INFINITY;
-      }
-      // Row max: eight independent chains of 3-input max, then a short tree.
-      float mx[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) mx[q] = fmax3(s[3 * q], s[3 * q + 1], s[3 * q + 2]);  // 0..23
-#pragma unroll
-      for (int cc = 24; cc < kBN - 8; cc += 16)
-#pragma unroll
-        for (int q = 0; q < 8; ++q) mx[q] = fmax3(mx[q], s[cc + 2 * q], s[cc + 2 * q + 1]);
-      // columns 24 .. 119 consumed; 120 .. 127 remain
-#pragma unroll
-      for (int q = 0; q < 8; ++q) mx[q] = fmaxf(mx[q], s[kBN - 8 + q]);
-      const float m_raw = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
-                                fmaxf(mx[6], mx[7]));
-      const float m_new = fmaxf(m2, m_raw * c);
-      float alpha = 1.f;
-      bool need = false;
-      if (m_new > m2 + kRescaleThreshold) {  // false while m_new == -inf
-        alpha = ex2_approx(m2 - m_new);      // 0 on the first visible tile
-        need = (j > 0);
-        m2 = m_new;
-      }
-      if (__any_sync(0xffffffffu, need)) {
-        // O_t row *= alpha before any of P_t,j is published.  PV_t,j-1
-        // completed before S_t,j was signalled.
+      const bool have_o = n_kv > 0 && l > 0.f;
+      const float inv_l = have_o ? p.o_scale / l : 0.f;
+      if constexpr (kPaged) {
+        // One unit per CTA: Q_t is dead and holds O_t for a TMA store.
+        uint8_t* s_o = s_q + t * C::kTileBytes;
 #pragma unroll 1
-        for (int cc = 0; cc < D; cc += 32) {
-          uint32_t o[32];
-          tmem_ld32_wait(lane_addr + col_o + cc, o);
+        for (int cc = 0; cc < D; cc += 64) {
+          uint32_t o[64] = {};
+          if (n_kv > 0) tmem_ld64_wait(lane_addr + col_o + cc, o);
+          uint8_t* sub = s_o + (cc / 64) * (kBM * 128) + r * 128;
 #pragma unroll
-          for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * alpha);
-          tmem_st32(lane_addr + col_o + cc, o);
-        }
-      }
-      const float mref = (m2 == -INFINITY) ? 0.f : m2;
-      const uint64_t c2 = f2_pack(c, c);
-      const uint64_t nm2 = f2_pack(-mref, -mref);
-      uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
+          for (int q = 0; q < 8; ++q) {  // 8 chunks of 8 columns = 16 bytes each
+            uint4 w;
+            uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        if constexpr (kFp8) {
-          uint32_t pk[16];  // 64 keys as E4M3, four per column
-#pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            float x0, x1, x2, x3;
-            f2_unpack(f2_fma(f2_pack(s[half * 64 + 4 * q], s[half * 64 + 4 * q + 1]), c2, nm2),
-                      x0, x1);
-            f2_unpack(f2_fma(f2_pack(s[half * 64 + 4 * q + 2], s[half * 64 + 4 * q + 3]), c2,
-                             nm2),
-                      x2, x3);
-            const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
-            const float e2 = ex2_approx(x2), e3 = ex2_approx(x3);
-            acc0 = f2_add(acc0, f2_pack(e0, e1));
-            acc1 = f2_add(acc1, f2_pack(e2, e3));
-            pk[q] = pack4_e4m3(e0, e1, e2, e3);
+            for (int e = 0; e < 4; ++e) {
+              const float v0 = have_o ? __uint_as_float(o[q * 8 + 2 * e]) * inv_l : 0.f;
+              const float v1 = have_o ? __uint_as_float(o[q * 8 + 2 * e + 1]) * inv_l : 0.f;
+              wp[e] = pack2<kBF16>(v0, v1);
+            }
+            *reinterpret_cast<uint4*>(sub + ((q ^ (r & 7)) * 16)) = w;
           }
-          tmem_st16(lane_addr + col_s + half * 16, pk);
-        } else {
-          uint32_t pk[32];
-#pragma unroll
-          for (int q = 0; q < 32; ++q) {
-            float x0, x1;
-            f2_unpack(f2_fma(f2_pack(s[half * 64 + 2 * q], s[half * 64 + 2 * q + 1]), c2, nm2),
-                      x0, x1);
-            const float e0 = ex2_approx(x0);
-            const float e1 = ex2_approx(x1);
-            if (q & 1)
-              acc1 = f2_add(acc1, f2_pack(e0, e1));
-            else
-              acc0 = f2_add(acc0, f2_pack(e0, e1));
-            pk[q] = pack2<kBF16>(e0, e1);
-          }
-          tmem_st32(lane_addr + col_s + half * 32, pk);
         }
-        tmem_st_wait();
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->p_half[t][half]);
-      }
-      float a0, a1, b0, b1;
-      f2_unpack(acc0, a0, a1);
-      f2_unpack(acc1, b0, b1);
-      l = l * alpha + ((a0 + a1) + (b0 + b1));
-    }
-
-    // ------------------------------------------------------------ epilogue
-    if (ok && n_all > 0)
-      ok = __all_sync(0xffffffffu, mbar_wait(&ctl->o_full, 0, p.wait_limit_ns, p.err, 40 + t));
-    tc_fence_after_sync();
-    const bool have_o = ok && n_kv(t) > 0 && l > 0.f;
-    const float inv_l = have_o ? p.o_scale / l : 0.f;
-    // 16-bit inputs: Q_t is dead once o_full fired and holds O_t; FP8: O has
-    // its own tiles.
-    uint8_t* s_o = kFp8 ? smem + C::kOStageOff + t * C::kOTileBytes : s_q + t * C::kTileBytes;
-#pragma unroll 1
-    for (int cc = 0; cc < D; cc += 64) {
-      uint32_t o[64] = {};
-      if (n_kv(t) > 0 && ok) tmem_ld64_wait(lane_addr + col_o + cc, o);
-      uint8_t* sub = s_o + (cc / 64) * (kBM * 128) + r * 128;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {  // 8 chunks of 8 columns = 16 bytes each
-        uint4 w;
-        uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float v0 = have_o ? __uint_as_float(o[q * 8 + 2 * e]) * inv_l : 0.f;
-          const float v1 = have_o ? __uint_as_float(o[q * 8 + 2 * e + 1]) * inv_l : 0.f;
-          wp[e] = pack2<kBF16>(v0, v1);
+        if (lane == 0) mbar_arrive(&ctl->o_free[t]);
+        fence_proxy_async_smem();
+        named_barrier_sync(1 + t, 128);
+        if (wl == 0 && lane == 0 && row0 < p.S_q) {
+          for (int x = 0; x < D / 64; ++x)
+            if (p.bshd)
+              tma_store_4d(&tm_o, s_o + x * (kBM * 128), x * 64, h, row0, b);
+            else
+              tma_store_4d(&tm_o, s_o + x * (kBM * 128), x * 64, row0, h, b);
+          tma_store_commit();
+          tma_store_wait_all();
         }
-        *reinterpret_cast<uint4*>(sub + ((q ^ (r & 7)) * 16)) = w;
+        __syncwarp();
+      } else {
+        // Q_t already holds the next unit's rows: O_t goes from registers
+        // straight to global memory, one 16-byte store per 8 columns of the
+        // thread's row, after the registers release tensor memory.
+        uint32_t o[D];
+#pragma unroll
+        for (int cc = 0; cc < D; cc += 64) {
+          if (n_kv > 0) {
+            tmem_ld64_wait(lane_addr + col_o + cc, *reinterpret_cast<uint32_t(*)[64]>(o + cc));
+          } else {
+#pragma unroll
+            for (int e = 0; e < 64; ++e) o[cc + e] = 0u;
+          }
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->o_free[t]);
+        if (i < p.S_q) {
+          // A row is D 16-bit values (128 or 256 bytes, 32-byte aligned):
+          // whole 32-byte sectors, one store each.
+          const size_t row = p.bshd ? (static_cast<size_t>(b) * p.S_q + i) * p.H + h
+                                    : (static_cast<size_t>(b) * p.H + h) * p.S_q + i;
+          uint16_t* dst = static_cast<uint16_t*>(p.o) + row * D;
+#pragma unroll
+          for (int q = 0; q < D / 16; ++q) {
+            uint32_t w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float v0 = have_o ? __uint_as_float(o[q * 16 + 2 * e]) * inv_l : 0.f;
+              const float v1 = have_o ? __uint_as_float(o[q * 16 + 2 * e + 1]) * inv_l : 0.f;
+              w[e] = pack2<kBF16>(v0, v1);
+            }
+            if (p.o_align32) {  // the base is 32-byte aligned (checked on the host)
+              st_global_v8(dst + q * 16, w);
+            } else {
+              uint4* d4 = reinterpret_cast<uint4*>(dst + q * 16);
+              d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+              d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            }
+          }
+        }
+      }
+      if (p.lse != nullptr && i < p.S_q) {
+        const float lse = have_o ? (m2 + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+        p.lse[(static_cast<size_t>(b) * p.H + h) * p.S_q + i] = lse;
       }
     }
     tc_fence_before_sync();
     __syncwarp();
     if (lane == 0) mbar_arrive(&ctl->tmem_free);
-    if (p.lse != nullptr && i < p.S_q) {
-      const float lse = have_o ? (m2 + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-      p.lse[(static_cast<size_t>(b) * p.H + h) * p.S_q + i] = lse;
-    }
-    fence_proxy_async_smem();
-    named_barrier_sync(1 + t, 128);
-    if (wl == 0 && lane == 0 && row0 < p.S_q) {
-      for (int x = 0; x < D / 64; ++x)
-        if (p.bshd)
-          tma_store_4d(&tm_o, s_o + x * (kBM * 128), x * 64, h, row0, b);
-        else
-          tma_store_4d(&tm_o, s_o + x * (kBM * 128), x * 64, row0, h, b);
-      tma_store_commit();
-      tma_store_wait_all();
-    }
-    __syncwarp();
   }
   // Stay resident until the partner has made its last multicast and commit.
   if (cs == 2) cluster_sync();
@@ -707,10 +879,17 @@ static cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const 
   return cudaLaunchKernelEx(&cfg, kern, q, k, v, o, p);
 }
 
+// Persistent CTAs (one per SM) when the host passes a zeroed scheduler
+// counter, else one CTA per unit.
+static int contiguous_grid(const PrefillParams& p) {
+  const int units = p.B * p.H * p.num_q_blocks;
+  return (p.sched != nullptr && p.ctas > 0 && p.ctas < units) ? p.ctas : units;
+}
+
 cudaError_t prefill_launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                            const CUtensorMap& o, const PrefillParams& p, int D, bool bf16,
                            cudaStream_t stream) {
-  const int grid = p.B * p.H * p.num_q_blocks;
+  const int grid = contiguous_grid(p);
   if (grid == 0) return cudaSuccess;
   if (D == 128) return bf16 ? launch_one<128, true, false>(q, k, v, o, p, grid, stream)
                             : launch_one<128, false, false>(q, k, v, o, p, grid, stream);
@@ -732,7 +911,7 @@ cudaError_t extend_launch(const CUtensorMap& q, const CUtensorMap& k, const CUte
 cudaError_t prefill_fp8_launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                const CUtensorMap& o, const PrefillParams& p, bool bf16_out,
                                cudaStream_t stream) {
-  const int grid = p.B * p.H * p.num_q_blocks;
+  const int grid = contiguous_grid(p);
   if (grid == 0) return cudaSuccess;
   return bf16_out ? launch_one<128, true, false, true>(q, k, v, o, p, grid, stream)
                   : launch_one<128, false, false, true>(q, k, v, o, p, grid, stream);

@@ -27,6 +27,11 @@ struct PrefillParams {
   const void* v_pool;
   int pair;                   // 1: CTA pairs (clusters of 2) share K/V tiles; needs an even group
   float o_scale;              // multiplies O at the end (the FP8 form's V descale, else 1)
+  // Contiguous forms only:
+  void* o;                    // O, 16-bit, q's layout (stored directly by the softmax warps)
+  int* sched;                 // zeroed unit counter: persistent CTAs; nullptr: one CTA per unit
+  int ctas;                   // persistent CTAs to launch (the SM count)
+  int o_align32;              // o is 32-byte aligned: whole-sector stores
 };
 
 // Tensor maps: 16-bit elements, 128-byte swizzle, box = 64 columns x

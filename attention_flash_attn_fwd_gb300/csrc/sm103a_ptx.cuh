@@ -522,6 +522,13 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
   return d;
 }
 
+// One 32-byte global store (a whole sector), 32-byte aligned address.
+__device__ __forceinline__ void st_global_v8(void* dst, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 // a * b clamped to [0, 1] (NaN -> 0) in the multiply itself
 __device__ __forceinline__ float mul_sat(float a, float b) {
   float d;

@@ -105,6 +105,60 @@ def test_prefill_is_deterministic():
     assert torch.equal(o1, o2)
 
 
+def test_persistent_and_per_unit_grids_agree_bitwise():
+    """Eager calls run persistent CTAs fed by the stream's unit counter; a
+    graph captured on a stream that never ran a prefill has no counter and
+    runs one CTA per unit.  Each unit is computed the same way either way."""
+    case = workloads.PrefillCase("grid", 3, 5, 777, 901, 128, "bshd", "bf16", True, seed=6)
+    q, k, v = (t.cuda() for t in workloads.make_prefill(case))
+    o_eager = attn.prefill(q, k, v, causal=True, layout="bshd")
+    out = torch.empty_like(o_eager)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        attn.prefill(q, k, v, causal=True, layout="bshd", out=out)
+    g.replay()
+    torch.cuda.synchronize()
+    assert attn.attn_device_error() == 0
+    assert torch.equal(o_eager, out)
+
+
+def test_concurrent_streams_use_their_own_unit_counters():
+    """Calls on two streams may overlap on the GPU: each stream's persistent
+    CTAs draw from that stream's counter, so both results are complete."""
+    cases = [workloads.PrefillCase("s%d" % n, 2, 8, 1024, 1024, 128, "bhsd", "fp16", n == 1,
+                                   seed=20 + n) for n in range(2)]
+    inputs = [tuple(t.cuda() for t in workloads.make_prefill(c)) for c in cases]
+    ref = [attn.prefill(*x, causal=c.causal) for x, c in zip(inputs, cases)]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in cases]
+    outs = [torch.empty_like(r) for r in ref]
+    for _ in range(3):
+        for st, x, c, o in zip(streams, inputs, cases, outs):
+            with torch.cuda.stream(st):
+                attn.prefill(*x, causal=c.causal, out=o)
+    torch.cuda.synchronize()
+    assert attn.attn_device_error() == 0
+    for o, r in zip(outs, ref):
+        assert torch.equal(o, r)
+
+
+def test_output_only_16_byte_aligned():
+    """An output 16 bytes into its allocation (16- but not 32-byte aligned)
+    is written with 16-byte stores and matches the aligned result."""
+    case = workloads.PrefillCase("al", 2, 3, 300, 300, 128, "bhsd", "bf16", True, seed=7)
+    q, k, v = (t.cuda() for t in workloads.make_prefill(case))
+    ref = attn.prefill(q, k, v, causal=True)
+    flat = torch.empty(ref.numel() + 8, device="cuda", dtype=ref.dtype)
+    out = flat[8:].view(ref.shape)
+    assert out.data_ptr() % 32 == 16
+    attn.prefill(q, k, v, causal=True, out=out)
+    torch.cuda.synchronize()
+    assert attn.attn_device_error() == 0
+    assert torch.equal(out, ref)
+
+
 def test_layouts_agree_bitwise():
     case = workloads.PrefillCase("lay", 2, 3, 333, 333, 128, "bhsd", "fp16", True, seed=4)
     q, k, v = (t.cuda() for t in workloads.make_prefill(case))
