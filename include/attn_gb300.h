@@ -77,6 +77,13 @@ typedef enum { ATTN_F16 = 0, ATTN_BF16 = 1 } attn_dtype;
  *   B, H, S_q, S_kv >= 0; B*H*S_q == 0 is a no-op.
  * Accumulation is fp32; P is rounded to the input dtype before P V; O is
  * rounded once, to nearest even.
+ * The library keeps one int per (device, stream), created on the stream's
+ * first call outside capture and zeroed on the stream before every launch:
+ * persistent CTAs take their query blocks from it.  A call captured on a
+ * stream that has none runs one CTA per query block (same results).  A
+ * captured graph must not be replayed concurrently with other prefill work
+ * of its capture stream (they share that counter).  attn_release_workspace
+ * frees these counters too.
  */
 ATTN_API attn_status attn_prefill_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                              int B, int H, int S_q, int S_kv, int D, attn_layout layout,
@@ -146,8 +153,8 @@ ATTN_API attn_status attn_prefill_bwd(const void* q, const void* k, const void* 
  *   o          output in out_dtype (ATTN_F16 or ATTN_BF16), q's shape and layout
  *   lse        [B,H,S_q] fp32 natural-log row sums of the real scores, or NULL
  *   descale_*  per-tensor factors, finite and > 0
- *   D          128 only (else ATTN_ERR_UNSUPPORTED); other arguments as for
- *              attn_prefill_fwd.
+ *   D          128 only (else ATTN_ERR_UNSUPPORTED); other arguments, and the
+ *              per-stream unit counter, as for attn_prefill_fwd.
  * Both products run on E4M3 operands with fp32 accumulation; P is rounded to
  * E4M3 (relative error up to 2^-4 per weight) before P V, which sets the
  * accuracy: about 2-3% relative L2 error on O for N(0,1) inputs, independent
@@ -285,8 +292,8 @@ ATTN_API attn_status attn_device_error(int* word, int clear);
  */
 ATTN_API void attn_set_wait_limit_ns(uint64_t ns);
 
-/* Free the decode workspaces (all streams) of the current device; synchronizes
- * the device (not during capture). */
+/* Free the decode workspaces and prefill unit counters (all streams) of the
+ * current device; synchronizes the device (not during capture). */
 ATTN_API attn_status attn_release_workspace(void);
 
 /* Library version string. */
