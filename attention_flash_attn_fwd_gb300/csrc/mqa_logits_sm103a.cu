@@ -260,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool live = __any_sync(0xffffffffu, slab_live(my_slo, my_shi, key0));
         bool ok = true;
         if (lane == 0 && tl >= kKRing)
-          ok = mbar_wait_sleep(&ctl->k_empty[stg], (tl / kKRing - 1) & 1, p.wait_limit_ns, p.err, 150);
+          ok = mbar_wait(&ctl->k_empty[stg], (tl / kKRing - 1) & 1, p.wait_limit_ns, p.err, 150);
         if (!__shfl_sync(0xffffffffu, ok, 0)) {
           if (lane == 0) *abort_flag = 1;
           break;
@@ -289,13 +289,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int tl = 0; tl < n_t && ok; ++tl) {
         const int stg = tl % kKRing;
         const int key0 = (t_begin + tl) * kKeys;
-        if (!(ok = mbar_wait_sleep(&ctl->k_full[stg], (tl / kKRing) & 1, p.wait_limit_ns, p.err, 161)))
+        if (!(ok = mbar_wait(&ctl->k_full[stg], (tl / kKRing) & 1, p.wait_limit_ns, p.err, 161)))
           break;
         const uint32_t k_lo = k_lo0 + ((stg * kTile) >> 4);
 #pragma unroll
         for (int s = 0; s < kSlabs; ++s) {
           const int v = tl * kSlabs + s, b = v % kBufs;
-          if (v >= kBufs && !(ok = mbar_wait_sleep(&ctl->t_empty[b], (v / kBufs - 1) & 1,
+          if (v >= kBufs && !(ok = mbar_wait(&ctl->t_empty[b], (v / kBufs - 1) & 1,
                                              p.wait_limit_ns, p.err, 162)))
             break;
           tc_fence_after_sync();

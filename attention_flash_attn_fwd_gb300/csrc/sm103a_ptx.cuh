@@ -95,37 +95,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   }
 }
 
-// try_wait with a suspend-time hint: a thread whose phase is not complete
-// sleeps (up to hint_ns) until it completes instead of spinning, leaving its
-// issue slots to the warps that have work.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
-                                                    uint32_t hint_ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
-      : "memory");
-  return ok != 0;
-}
-
-// mbar_wait for waits that are usually long: the same bound, but each try
-// sleeps up to 20 us.
-__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
-                                                int* err, int site) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (;;) {
-    if (mbar_try_wait_sleep(bar, parity, 20000)) return true;
-    if (globaltimer_ns() - t0 > limit_ns) {
-      record_error(err, kErrWaitTimeout, site);
-      return false;
-    }
-  }
-}
-
 // --------------------------------------------------------------- proxies
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
