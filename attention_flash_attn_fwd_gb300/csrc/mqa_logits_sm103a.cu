@@ -113,14 +113,15 @@ __device__ __forceinline__ KeyScale key_scale(float scale) {
   return k;
 }
 
-// For a key scale >= 0, relu(scale * x) = scale * relu(x): the head sum is
-// taken over relu(x) and scaled once.  relu of a float is a signed-integer
+// The fast path splits the ReLU between two pipes.  Key g (scale >= 0):
+// relu(scale * x) = scale * relu(x), and relu of a float is a signed-integer
 // max with 0 on its bits (negative floats, -0 included, are negative
-// integers), one ALU instruction that leaves the FMA pipe to a packed
-// f32x2 FMA over the column pairs the load already delivers adjacent.
+// integers) on the ALU pipe; its head sum is scaled once.  Key g + 8: the
+// exact saturating multiply on the FMA pipe (see KeyScale).  Both feed a
+// packed f32x2 FMA over the column pairs the load already delivers adjacent.
 template <int H>
 __device__ __forceinline__ void accumulate_half_pos(const float (&v)[64], const float* w_slab, int c,
-                                                    uint64_t (&a)[kCols / H][2]) {
+                                                    float s_sat1, uint64_t (&a)[kCols / H][2]) {
 #pragma unroll
   for (int r = 0; r < 16; ++r) {
     const int row = (8 * r) / H;
@@ -128,8 +129,8 @@ __device__ __forceinline__ void accumulate_half_pos(const float (&v)[64], const 
     const uint64_t wp = f2_pack(w2.x, w2.y);
     const float y0 = __int_as_float(max(__float_as_int(v[4 * r]), 0));
     const float y1 = __int_as_float(max(__float_as_int(v[4 * r + 1]), 0));
-    const float y2 = __int_as_float(max(__float_as_int(v[4 * r + 2]), 0));
-    const float y3 = __int_as_float(max(__float_as_int(v[4 * r + 3]), 0));
+    const float y2 = mul_sat(v[4 * r + 2], s_sat1);
+    const float y3 = mul_sat(v[4 * r + 3], s_sat1);
     a[row][0] = f2_fma(f2_pack(y0, y1), wp, a[row][0]);
     a[row][1] = f2_fma(f2_pack(y2, y3), wp, a[row][1]);
   }
@@ -354,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_units = n_t * kSlabs;
     KeyScale ks[2][2];
     float kraw[2][2];
-    bool sat = true, pos = true;
+    bool sat = true, pos = true, fast = true;
     int cur_tl = -1;
     for (int v = wg; v < n_units && ok; v += kEpiGroups) {
       const int tl = v / kSlabs, s = v % kSlabs, b = v % kBufs;
@@ -377,6 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the barrier arrive, which the whole warp must reach together.
         pos = __all_sync(0xffffffffu, pos);
         sat = __all_sync(0xffffffffu, sat);
+        fast = pos && sat;
       }
       ok = __all_sync(0xffffffffu,
                       mbar_wait(&ctl->s_full[b], (v / kBufs) & 1, p.wait_limit_ns, p.err, 170));
@@ -386,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float u[2][R][2];  // [half][row][key of the pair]: this thread's partial head sums
       const float* w_slab = stats->w + s * kCols;
       const uint32_t taddr = lane_addr + kCols * b;
-      if (live && pos) {
+      if (live && fast) {
         uint64_t a2[2][R][2];
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf)
@@ -394,13 +396,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int r = 0; r < R; ++r) a2[hf][r][0] = a2[hf][r][1] = f2_pack(0.f, 0.f);
         float x[64];
         tmem_ld16x256b_x16_wait(taddr, x);
-        accumulate_half_pos<H>(x, w_slab, c, a2[0]);
+        accumulate_half_pos<H>(x, w_slab, c, ks[0][1].s_sat, a2[0]);
         tmem_ld16x256b_x16_wait(taddr + (16u << 16), x);
         // The whole buffer is in registers: hand it back.
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl->t_empty[b]);
-        accumulate_half_pos<H>(x, w_slab, c, a2[1]);
+        accumulate_half_pos<H>(x, w_slab, c, ks[1][1].s_sat, a2[1]);
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
@@ -465,7 +467,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         z[r] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
       }
       const float unscale =
-          pos ? ((c & 2) ? ((c & 1) ? kraw[1][1] : kraw[1][0]) : ((c & 1) ? kraw[0][1] : kraw[0][0]))
+          fast ? ((c & 2) ? ((c & 1) ? ks[1][1].unscale : kraw[1][0])
+                          : ((c & 1) ? ks[0][1].unscale : kraw[0][0]))
               : ((c & 2) ? ((c & 1) ? ks[1][1].unscale : ks[1][0].unscale)
                          : ((c & 1) ? ks[0][1].unscale : ks[0][0].unscale));
       const int j = key0 + j_off;
