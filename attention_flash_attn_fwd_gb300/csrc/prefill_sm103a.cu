@@ -31,8 +31,10 @@
 //    faster CTAs take more of the unequal causal units.  Between units nothing
 //    drains: Q_t is refilled once the unit's last S MMA of tile t has read it,
 //    K/V keep streaming through the same ring, the next unit's first S MMAs
-//    run during the epilogue, and O leaves in whole-sector stores straight
-//    from registers (Q's tiles already hold the next unit).  Measured on
+//    run during the epilogue, and O leaves without touching Q's tiles (which
+//    already hold the next unit): by TMA store from staging tiles of its own
+//    where shared memory has room (FP8, D = 64), else in whole-sector stores
+//    straight from registers.  Measured on
 //    GB300, the one-unit CTAs spent ~5.8 us per unit outside the main loop
 //    (set-up, the first Q/K tiles arriving, epilogue, CTA turnover).
 //
@@ -86,7 +88,7 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 constexpr int kCtlBytesFwd = 512;  // reserved for SharedCtl (checked below)
 
-template <int D, bool kFp8 = false>
+template <int D, bool kFp8 = false, bool kPaged = false>
 struct Cfg {
   static constexpr int kElt = kFp8 ? 1 : 2;               // bytes per Q/K/V element
   static constexpr int kTileBytes = kBM * D * kElt;       // one Q/K/V tile
@@ -95,9 +97,13 @@ struct Cfg {
   static constexpr int kBoxes = D / kBoxCols;             // boxes (swizzle panels) per row
   static constexpr int kKeysPerPV = 32 / kElt;            // keys per PV MMA instruction
   static constexpr int kStages = kFp8 ? 8 : ((D == 128) ? 5 : 10);  // KV ring depth
-  // FP8: O has its own staging tiles (a Q tile is too small to hold it).
+  // O leaves the contiguous forms by TMA store from staging tiles of their own
+  // where shared memory has room for them (FP8, D = 64); at D = 128 in 16
+  // bits the 5-stage ring fills shared memory and O is stored straight from
+  // registers (measured faster there than staging with a shallower ring).
+  static constexpr bool kStagedO = !kPaged && (kFp8 || D == 64);
   static constexpr int kOStageOff = kTiles * kTileBytes + kStages * kTileBytes;
-  static constexpr int kSmemData = kOStageOff + (kFp8 ? kTiles * kOTileBytes : 0);
+  static constexpr int kSmemData = kOStageOff + (kStagedO ? kTiles * kOTileBytes : 0);
   static constexpr int kSmemBytes = kSmemData + 1024 /*align*/ + kCtlBytesFwd;
   // tensor-memory columns of S_t and O_t
   __device__ static constexpr uint32_t col_s(int t) { return t * 128u; }
@@ -291,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_o, const PrefillParams p) {
-  using C = Cfg<D, kFp8>;
+  using C = Cfg<D, kFp8, kPaged>;
   extern __shared__ uint8_t smem_raw[];
   // Offset from the __shared__ array, so accesses stay in the shared space.
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -786,43 +792,95 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       } else {
-        // Q_t already holds the next unit's rows: O_t goes from registers
-        // straight to global memory, one 16-byte store per 8 columns of the
-        // thread's row, after the registers release tensor memory.
-        uint32_t o[D];
+        if constexpr (C::kStagedO) {
+          // O_t is staged in this query tile's own shared-memory tile (Q_t
+          // already holds the next unit) and leaves by TMA store.  The thread
+          // that issues the store first waits until its previous store has
+          // read the tile; the loads from tensor memory run meanwhile.
+          uint8_t* s_o = smem + C::kOStageOff + t * C::kOTileBytes;
+          const bool issuer = wl == 0 && lane == 0;
+          uint32_t o[D];
 #pragma unroll
-        for (int cc = 0; cc < D; cc += 64) {
-          if (n_kv > 0) {
-            tmem_ld64_wait(lane_addr + col_o + cc, *reinterpret_cast<uint32_t(*)[64]>(o + cc));
-          } else {
-#pragma unroll
-            for (int e = 0; e < 64; ++e) o[cc + e] = 0u;
-          }
-        }
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->o_free[t]);
-        if (i < p.S_q) {
-          // A row is D 16-bit values (128 or 256 bytes, 32-byte aligned):
-          // whole 32-byte sectors, one store each.
-          const size_t row = p.bshd ? (static_cast<size_t>(b) * p.S_q + i) * p.H + h
-                                    : (static_cast<size_t>(b) * p.H + h) * p.S_q + i;
-          uint16_t* dst = static_cast<uint16_t*>(p.o) + row * D;
-#pragma unroll
-          for (int q = 0; q < D / 16; ++q) {
-            uint32_t w[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float v0 = have_o ? __uint_as_float(o[q * 16 + 2 * e]) * inv_l : 0.f;
-              const float v1 = have_o ? __uint_as_float(o[q * 16 + 2 * e + 1]) * inv_l : 0.f;
-              w[e] = pack2<kBF16>(v0, v1);
-            }
-            if (p.o_align32) {  // the base is 32-byte aligned (checked on the host)
-              st_global_v8(dst + q * 16, w);
+          for (int cc = 0; cc < D; cc += 64) {
+            if (n_kv > 0) {
+              tmem_ld64_wait(lane_addr + col_o + cc, *reinterpret_cast<uint32_t(*)[64]>(o + cc));
             } else {
-              uint4* d4 = reinterpret_cast<uint4*>(dst + q * 16);
-              d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-              d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+#pragma unroll
+              for (int e = 0; e < 64; ++e) o[cc + e] = 0u;
+            }
+          }
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl->o_free[t]);
+          if (issuer) tma_store_wait_read_all();
+          named_barrier_sync(1 + t, 128);
+#pragma unroll
+          for (int cc = 0; cc < D; cc += 64) {
+            uint8_t* sub = s_o + (cc / 64) * (kBM * 128) + r * 128;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {  // 8 chunks of 8 columns = 16 bytes each
+              uint4 w;
+              uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float v0 = have_o ? __uint_as_float(o[cc + q * 8 + 2 * e]) * inv_l : 0.f;
+                const float v1 =
+                    have_o ? __uint_as_float(o[cc + q * 8 + 2 * e + 1]) * inv_l : 0.f;
+                wp[e] = pack2<kBF16>(v0, v1);
+              }
+              *reinterpret_cast<uint4*>(sub + ((q ^ (r & 7)) * 16)) = w;
+            }
+          }
+          fence_proxy_async_smem();
+          named_barrier_sync(1 + t, 128);
+          if (issuer && row0 < p.S_q) {
+            for (int x = 0; x < D / 64; ++x)
+              if (p.bshd)
+                tma_store_4d(&tm_o, s_o + x * (kBM * 128), x * 64, h, row0, b);
+              else
+                tma_store_4d(&tm_o, s_o + x * (kBM * 128), x * 64, row0, h, b);
+            tma_store_commit();
+          }
+          __syncwarp();
+        } else {
+          // Q_t already holds the next unit's rows: O_t goes from registers
+          // straight to global memory, one 16-byte store per 8 columns of the
+          // thread's row, after the registers release tensor memory.
+          uint32_t o[D];
+#pragma unroll
+          for (int cc = 0; cc < D; cc += 64) {
+            if (n_kv > 0) {
+              tmem_ld64_wait(lane_addr + col_o + cc, *reinterpret_cast<uint32_t(*)[64]>(o + cc));
+            } else {
+#pragma unroll
+              for (int e = 0; e < 64; ++e) o[cc + e] = 0u;
+            }
+          }
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl->o_free[t]);
+          if (i < p.S_q) {
+            // A row is D 16-bit values (128 or 256 bytes, 32-byte aligned):
+            // whole 32-byte sectors, one store each.
+            const size_t row = p.bshd ? (static_cast<size_t>(b) * p.S_q + i) * p.H + h
+                                      : (static_cast<size_t>(b) * p.H + h) * p.S_q + i;
+            uint16_t* dst = static_cast<uint16_t*>(p.o) + row * D;
+#pragma unroll
+            for (int q = 0; q < D / 16; ++q) {
+              uint32_t w[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const float v0 = have_o ? __uint_as_float(o[q * 16 + 2 * e]) * inv_l : 0.f;
+                const float v1 = have_o ? __uint_as_float(o[q * 16 + 2 * e + 1]) * inv_l : 0.f;
+                w[e] = pack2<kBF16>(v0, v1);
+              }
+              if (p.o_align32) {  // the base is 32-byte aligned (checked on the host)
+                st_global_v8(dst + q * 16, w);
+              } else {
+                uint4* d4 = reinterpret_cast<uint4*>(dst + q * 16);
+                d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+              }
             }
           }
         }
@@ -832,6 +890,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         p.lse[(static_cast<size_t>(b) * p.H + h) * p.S_q + i] = lse;
       }
     }
+    // No O store may still be reading shared memory when the CTA exits.
+    if (C::kStagedO && wl == 0 && lane == 0) tma_store_wait_all();
     tc_fence_before_sync();
     __syncwarp();
     if (lane == 0) mbar_arrive(&ctl->tmem_free);
@@ -856,18 +916,18 @@ static cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const 
     if (e != cudaSuccess) return e;
     if (fa.numRegs != kRegsAtLaunch) return cudaErrorInvalidConfiguration;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg<D, kFp8>::kSmemBytes);
+                             Cfg<D, kFp8, kPaged>::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   if (!(kPaged && p.pair)) {
-    kern<<<grid, kThreads, Cfg<D, kFp8>::kSmemBytes, stream>>>(q, k, v, o, p);
+    kern<<<grid, kThreads, Cfg<D, kFp8, kPaged>::kSmemBytes, stream>>>(q, k, v, o, p);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Cfg<D, kFp8>::kSmemBytes;
+  cfg.dynamicSmemBytes = Cfg<D, kFp8, kPaged>::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
