@@ -46,6 +46,7 @@ _STATUS_NAMES = {
 EXPORTED = ("attn_prefill_fwd", "attn_prefill_bwd", "attn_mqa_logits_fp8", "attn_prefill_fp8_fwd", "attn_extend_fwd", "attn_decode_fwd", "attn_decode_fwd_noalloc",
             "attn_last_error",
             "attn_device_error", "attn_set_wait_limit_ns", "attn_release_workspace",
+            "attn_selftest_wait_timeout",
             "attn_version")
 
 
@@ -98,6 +99,8 @@ def lib() -> ctypes.CDLL:
             L.attn_device_error.restype = ci
             L.attn_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
             L.attn_set_wait_limit_ns.restype = None
+            L.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+            L.attn_selftest_wait_timeout.restype = ci
             L.attn_release_workspace.argtypes = []
             L.attn_release_workspace.restype = ci
             L.attn_version.argtypes = []
@@ -189,6 +192,12 @@ def attn_device_error(clear: bool = True) -> int:
 
 def attn_set_wait_limit_ns(ns: int) -> None:
     lib().attn_set_wait_limit_ns(ns)
+
+
+def attn_selftest_wait_timeout(limit_ns: int, stream=None) -> None:
+    """Launch a wait that nothing completes; after ``limit_ns`` it records a
+    timeout (site 900) in the device error word."""
+    _check(lib().attn_selftest_wait_timeout(limit_ns, _stream_handle(stream)))
 
 
 def attn_release_workspace() -> int:

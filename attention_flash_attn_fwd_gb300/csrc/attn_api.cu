@@ -17,6 +17,7 @@
 #include "decode_sm103a.h"
 #include "mqa_logits_sm103a.h"
 #include "prefill_sm103a.h"
+#include "sm103a_ptx.cuh"
 #include "tmap.h"
 
 namespace {
@@ -91,6 +92,18 @@ attn_status prefill_sched(DeviceState* st, cudaStream_t stream, int** out) {
 }
 
 DeviceState g_dev[kMaxDevices];
+
+// A wait that nothing completes: one thread initialises an mbarrier nobody
+// arrives on and waits for its first phase with the kernels' bounded wait,
+// which gives up after limit_ns and records (timeout << 16) | kSelftestSite
+// in the error word.  No copy, MMA or tensor memory is involved.
+constexpr int kSelftestSite = 900;
+__global__ void selftest_wait_kernel(int* err, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  attn_sm103a::mbar_init(&bar, 1);
+  attn_sm103a::fence_mbar_init();
+  attn_sm103a::mbar_wait(&bar, 0, limit_ns, err, kSelftestSite);
+}
 
 // Per-device set-up, done once with the device current.
 attn_status device_state(DeviceState** out) {
@@ -204,6 +217,18 @@ const char* attn_last_error(void) { return t_last_error.c_str(); }
 
 void attn_set_wait_limit_ns(uint64_t ns) {
   g_wait_limit_ns.store(ns ? ns : initial_wait_limit());
+}
+
+attn_status attn_selftest_wait_timeout(uint64_t limit_ns, cudaStream_t stream) {
+  if (limit_ns == 0 || limit_ns > 10000000000ull)
+    return fail(ATTN_ERR_INVALID_ARG, "limit_ns must be in (0, 1e10]");
+  DeviceState* st = nullptr;
+  attn_status s = device_state(&st);
+  if (s != ATTN_OK) return s;
+  selftest_wait_kernel<<<1, 1, 0, stream>>>(st->err_word, limit_ns);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail_cuda(e, "self-test launch");
+  return ATTN_OK;
 }
 
 attn_status attn_device_error(int* word, int clear) {

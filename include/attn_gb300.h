@@ -292,6 +292,16 @@ ATTN_API attn_status attn_device_error(int* word, int clear);
  */
 ATTN_API void attn_set_wait_limit_ns(uint64_t ns);
 
+/*
+ * Failure-detection self-test: launches one thread that waits, with the same
+ * bounded wait every kernel uses, on an mbarrier nothing ever completes.
+ * After limit_ns (0 < limit_ns <= 1e10) the wait gives up and records
+ * (1 << 16) | 900 (a timed-out wait at site 900) in the device error word,
+ * which attn_device_error() then reports; the context stays usable.
+ * Returns ATTN_ERR_INVALID_ARG for a limit out of range.
+ */
+ATTN_API attn_status attn_selftest_wait_timeout(uint64_t limit_ns, cudaStream_t stream);
+
 /* Free the decode workspaces and prefill unit counters (all streams) of the
  * current device; synchronizes the device (not during capture). */
 ATTN_API attn_status attn_release_workspace(void);

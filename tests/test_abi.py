@@ -242,3 +242,8 @@ def test_product_never_imports_the_oracle():
                     text = f.read()
                 for bad in ("import oracle", "from oracle", "liboracle", "attn_oracle"):
                     assert bad not in text, (fn, bad)
+
+
+@pytest.mark.parametrize("limit", [0, 10_000_000_001])
+def test_selftest_wait_rejects_limits_out_of_range(limit):
+    assert attn.lib().attn_selftest_wait_timeout(limit, None) == attn.ATTN_ERR_INVALID_ARG
