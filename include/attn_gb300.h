@@ -247,8 +247,8 @@ ATTN_API attn_status attn_decode_fwd(const void* q, const void* k_pool, const vo
                             cudaStream_t stream);
 
 /*
- * Decode attention that allocates no device memory (no counterpart in the
- * paper: the pages never discuss workspace ownership).
+ * Decode attention that allocates no device memory (no counterpart on the
+ * source pages, which never discuss workspace ownership).
  *
  * Same arguments, rules and results as attn_decode_fwd, for callers that must
  * not let a library allocate: code being captured into a CUDA graph, engines
