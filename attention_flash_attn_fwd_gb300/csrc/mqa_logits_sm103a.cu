@@ -14,15 +14,17 @@
 // 128-key tiles that a producer warp streams through a 4-stage ring (the
 // page's split of the key axis across the grid).  Per (key tile, slab) one
 // tcgen05.mma .kind::f8f6f4 chain computes S^T = K_tile Q_slab^T, M = 128 keys
-// by N = 128 pairs, into one of four 128-column tensor-memory buffers; the two
-// epilogue warpgroups take alternate slabs, so each has two buffers in flight.
+// by N = 128 pairs, into one of four 128-column tensor-memory buffers; three
+// epilogue warpgroups take the (tile, slab) units round-robin, so the MMA runs
+// ahead while a sub-partition's three epilogue warps hide each other's loads.
 //
 // Epilogue: each warp reads its 32 keys of a buffer as two 16x256b loads, so
 // a thread holds 4 keys x 32 of the slab's 128 columns and every weight it
-// reads from shared memory serves 4 keys.  ReLU and the per-key scale are one
-// saturating multiply per element (see below), the weighted sum a packed FMA,
-// and two shuffle steps finish the head sum across the 4 threads that share
-// a key.  Stores run along the key axis (128 contiguous bytes per row and
+// reads from shared memory serves 4 keys.  The ReLU is split across two pipes
+// (an integer max on the ALU for one key of a register pair, an exact
+// saturating multiply on the FMA pipe for the other; see KeyScale), the
+// weighted sum is a packed FMA, and two shuffle steps finish the head sum
+// across the 4 threads that share a key.  Stores run along the key axis (128 contiguous bytes per row and
 // warp).  A (tile, slab) pair none of whose rows' windows meets the tile is
 // neither multiplied nor read back (the page's tile_skip / empty-window fix);
 // a tile no slab needs is not even loaded.  Every wait is bounded.
