@@ -35,16 +35,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ bool elect_one_lane() {
-  uint32_t pred = 0;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "elect.sync _|p, 0xffffffff;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(pred));
-  return pred != 0;
-}
-
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
@@ -153,16 +143,6 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
-__device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                            int c0, int c1, int c2, int c3, int c4) {
-  asm volatile(
-      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
-      "r"(smem_u32(bar))
-      : "memory");
-}
-
 // Prefetch one box of a tiled tensor into L2 (no shared memory, no barrier).
 __device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap* map, int c0, int c1, int c2,
                                                    int c3) {
@@ -221,26 +201,16 @@ __device__ __forceinline__ void tc_fence_after_sync() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor for a 128-byte-swizzled operand tile
-// (tcgen05 "version 1" descriptor).  lbo/sbo are byte strides:
-//  * K-major (rows of 64 16-bit elements): sbo = stride between 8-row groups,
-//    lbo unused;
-//  * MN-major: lbo = stride between 64-element groups along M/N, sbo = stride
-//    between 8-row groups along K.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
-  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
-  d |= static_cast<uint64_t>(1) << 46;  // descriptor version for tcgen05
-  d |= static_cast<uint64_t>(2) << 61;  // 128-byte swizzle
-  return d;
-}
-
-// The same descriptor split into 32-bit halves, so a loop can step the
-// start address with one add on the low word.  Shared-memory addresses are
-// below 2^18, so (addr >> 4) fits the 14-bit field with no carry into the
-// leading-byte-offset bits.
+// Shared-memory matrix descriptor of a 128-byte-swizzled operand tile (the
+// tcgen05 descriptor, version 1), as two 32-bit halves so a loop can step the
+// start address with one add on the low word.  Low word: start address >> 4,
+// leading byte offset >> 4 at bit 16.  High word: stride byte offset >> 4,
+// the version at bit 14 (bit 46 of the descriptor), 128-byte swizzle (2) at
+// bit 29 (61).  K-major operands (rows of 128 bytes): sbo = stride between
+// 8-row groups, lbo unused; MN-major: lbo = stride between 128-byte column
+// groups, sbo = stride between 8-row groups along K.  Shared-memory addresses
+// are below 2^18, so (addr >> 4) fits its 14-bit field with no carry into
+// the leading-byte-offset bits.
 __device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo) {
   return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
 }
@@ -260,7 +230,6 @@ __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, int M, int N, bool a
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
-// D[tmem] (+)= A[smem] * B[smem]
 // Instruction descriptor of `.kind::f8f6f4` with E4M3 A and B (format code 0)
 // and an f32 accumulator.
 __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, bool a_mn_major,
@@ -274,28 +243,8 @@ __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, bool a_mn_major,
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Same MMAs with the shared-memory descriptors given as 32-bit halves.
+// D[tmem] (+)= A[smem] * B[smem], the shared-memory descriptors given as
+// 32-bit halves (callers build them once and add offsets to the low word).
 // kF8: `.kind::f8f6f4` (8-bit A and B; K = 32 per instruction) instead of
 // `.kind::f16` (K = 16).
 template <bool kF8 = false>
@@ -323,6 +272,7 @@ __device__ __forceinline__ void mma_ss_lh(uint32_t d_tmem, uint32_t a_lo, uint32
   }
 }
 
+// D[tmem] (+)= A[tmem] * B[smem] (A read from tensor memory).
 template <bool kF8 = false>
 __device__ __forceinline__ void mma_ts_lh(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
                                           uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
@@ -488,12 +438,6 @@ __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
 __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   uint64_t d;
   asm("add.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("mul.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
 
