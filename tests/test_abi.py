@@ -247,3 +247,45 @@ def test_product_never_imports_the_oracle():
 @pytest.mark.parametrize("limit", [0, 10_000_000_001])
 def test_selftest_wait_rejects_limits_out_of_range(limit):
     assert attn.lib().attn_selftest_wait_timeout(limit, None) == attn.ATTN_ERR_INVALID_ARG
+
+
+def test_no_fallback_when_the_library_cannot_be_built():
+    """A missing toolkit or library is an error, never a silent host path."""
+    code = (
+        "import attention_flash_attn_fwd_gb300 as a\n"
+        "from attention_flash_attn_fwd_gb300 import _build\n"
+        "def no_nvcc(*args, **kw):\n"
+        "    raise RuntimeError('nvcc not found')\n"
+        "_build.build = no_nvcc\n"
+        "try:\n"
+        "    a.lib()\n"
+        "except RuntimeError as e:\n"
+        "    print('raised', e)\n"
+        "else:\n"
+        "    print('loaded')\n")
+    r = subprocess.run(["python", "-c", code], capture_output=True, text=True, cwd=ROOT,
+                       timeout=300)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == "raised nvcc not found"
+
+
+@pytest.mark.parametrize("form", ["prefill", "prefill_bwd", "extend", "decode"])
+def test_wrappers_reject_host_tensors(form):
+    import torch
+    q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        if form == "prefill":
+            attn.prefill(q, q, q)
+        elif form == "prefill_bwd":
+            lse = torch.zeros(1, 1, 128, dtype=torch.float32)
+            attn.prefill_bwd(q, q, q, q, q, lse)
+        elif form == "extend":
+            pool = torch.zeros(4, 16, 1, 64, dtype=torch.bfloat16)
+            lens = torch.full((1,), 64, dtype=torch.int32)
+            table = torch.arange(4, dtype=torch.int32).view(1, 4)
+            attn.extend(q.view(1, 128, 1, 64)[:, :16], pool, pool, table, lens)
+        else:
+            pool = torch.zeros(4, 16, 1, 64, dtype=torch.bfloat16)
+            lens = torch.full((1,), 64, dtype=torch.int32)
+            table = torch.arange(4, dtype=torch.int32).view(1, 4)
+            attn.decode(q.view(1, 128, 64)[:, :1], pool, pool, lens, page_table=table)
