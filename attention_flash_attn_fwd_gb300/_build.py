@@ -17,8 +17,8 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libattn_gb300.so")
 SOURCES = ["attn_api.cu", "prefill_sm103a.cu", "decode_sm103a.cu", "attn_noalloc.cu",
            "backward_sm103a.cu", "mqa_logits_sm103a.cu"]
-HEADERS = ["sm103a_ptx.cuh", "tmap.h", "prefill_sm103a.h", "decode_sm103a.h",
-           "backward_sm103a.h", "mqa_logits_sm103a.h"]
+HEADERS = ["sm103a_ptx.cuh", "tmap.h", "host_once.h", "prefill_sm103a.h", "decode_sm103a.h",
+           "backward_sm103a.h", "mqa_logits_sm103a.h", "decode_plan.h"]
 GENCODE = "arch=compute_103a,code=sm_103a"
 
 

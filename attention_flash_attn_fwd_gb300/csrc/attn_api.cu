@@ -11,9 +11,11 @@
 #include <mutex>
 #include <string>
 #include <unordered_map>
+#include <vector>
 
 #include "../../include/attn_gb300.h"
 #include "backward_sm103a.h"
+#include "decode_plan.h"
 #include "decode_sm103a.h"
 #include "mqa_logits_sm103a.h"
 #include "prefill_sm103a.h"
@@ -60,6 +62,9 @@ struct DeviceState {
     size_t bytes = 0;
   };
   std::unordered_map<cudaStream_t, Workspace> workspaces;
+  // Buffers a workspace outgrew: still referenced by any graph captured while
+  // they were current, so kept until attn_release_workspace.
+  std::vector<void*> retired;
   // Prefill unit counters (one int per stream): persistent CTAs take their
   // next query block from it; the host zeroes it before every launch.
   std::unordered_map<cudaStream_t, int*> sched;
@@ -604,6 +609,83 @@ attn_status attn_decode_fwd(const void* q, const void* k_pool, const void* v_poo
                             int H_q, int H_kv, int D, int page_size, int max_pages_per_seq,
                             int num_pages, int num_splits, float scale, attn_dtype dtype,
                             cudaStream_t stream) {
+  attn_internal::DecodePlan plan;
+  attn_status s = attn_internal::decode_plan(q, k_pool, v_pool, page_table, kv_lens, o, B, H_q,
+                                             H_kv, D, page_size, max_pages_per_seq, num_pages,
+                                             num_splits, scale, dtype, &plan);
+  if (s != ATTN_OK || plan.empty) return s;
+  DeviceState* st = nullptr;
+  s = device_state(&st);
+  if (s != ATTN_OK) return s;
+
+  // The stream's workspace.  A graph captured earlier may hold the current
+  // buffer's address, so a buffer that has to grow is retired, not freed:
+  // retired buffers are freed by attn_release_workspace.  Growth is at least
+  // 2x, so retired buffers add up to less than the live one.
+  const size_t need = plan.partial_bytes;
+  void* workspace = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(st->mu);
+    DeviceState::Workspace& w = st->workspaces[stream];
+    if (w.bytes < need) {
+      cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+      cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+      if (e != cudaSuccess) return fail_cuda(e, "cudaStreamIsCapturing");
+      if (cs != cudaStreamCaptureStatusNone)
+        return fail(ATTN_ERR_NO_MEMORY,
+                    "decode workspace must grow but the stream is capturing; call once before "
+                    "capture with the largest shapes");
+      const size_t bytes = need > 2 * w.bytes ? need : 2 * w.bytes;
+      void* ws = nullptr;
+      e = cudaMalloc(&ws, bytes);
+      if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(ATTN_ERR_NO_MEMORY, std::string("workspace cudaMalloc: ") + cudaGetErrorString(e));
+      }
+      if (w.ptr) st->retired.push_back(w.ptr);
+      w.ptr = ws;
+      w.bytes = bytes;
+    }
+    workspace = w.ptr;
+  }
+  return attn_internal::decode_enqueue(plan, static_cast<float*>(workspace), stream);
+}
+
+attn_status attn_release_workspace(void) {
+  DeviceState* st = nullptr;
+  attn_status s = device_state(&st);
+  if (s != ATTN_OK) return s;
+  std::lock_guard<std::mutex> lk(st->mu);
+  if (!st->workspaces.empty() || !st->retired.empty()) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceSynchronize");
+    for (auto& kv : st->workspaces) cudaFree(kv.second.ptr);
+    st->workspaces.clear();
+    for (void* ptr : st->retired) cudaFree(ptr);
+    st->retired.clear();
+  }
+  if (!st->sched.empty()) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceSynchronize");
+    for (auto& kv : st->sched) cudaFree(kv.second);
+    st->sched.clear();
+  }
+  return ATTN_OK;
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------------
+// The decode plan shared by attn_decode_fwd and attn_decode_fwd_noalloc.
+namespace attn_internal {
+
+attn_status set_error(attn_status s, const char* msg) { return fail(s, msg); }
+
+attn_status decode_plan(const void* q, const void* k_pool, const void* v_pool,
+                        const int32_t* page_table, const int32_t* kv_lens, void* o, int B,
+                        int H_q, int H_kv, int D, int page_size, int max_pages_per_seq,
+                        int num_pages, int num_splits, float scale, attn_dtype dtype,
+                        DecodePlan* plan) {
   if (B < 0) return fail(ATTN_ERR_INVALID_ARG, "B must be >= 0");
   if (H_q <= 0 || H_kv <= 0) return fail(ATTN_ERR_INVALID_ARG, "H_q and H_kv must be > 0");
   if (H_q % H_kv != 0) return fail(ATTN_ERR_INVALID_ARG, "H_q must be a multiple of H_kv");
@@ -627,6 +709,7 @@ attn_status attn_decode_fwd(const void* q, const void* k_pool, const void* v_poo
     if (num_pages != B)
       return fail(ATTN_ERR_INVALID_ARG, "contiguous cache: num_pages must equal B");
   }
+  plan->empty = B == 0;
   if (B == 0) return ATTN_OK;
   if (!q || !k_pool || !v_pool || !kv_lens || !o)
     return fail(ATTN_ERR_INVALID_ARG, "q, k_pool, v_pool, kv_lens and o must be non-NULL");
@@ -665,114 +748,46 @@ attn_status attn_decode_fwd(const void* q, const void* k_pool, const void* v_poo
   if (static_cast<int64_t>(max_splits) > 65535)
     return fail(ATTN_ERR_UNSUPPORTED, "too many splits for one launch");
 
-  // Workspace: o_part [B, H_q, max_splits, D] + lse_part [B, H_q, max_splits].
-  const size_t rows_ws = static_cast<size_t>(B) * H_q * max_splits;
-  const size_t need = rows_ws * D * sizeof(float) + rows_ws * sizeof(float);
-  void* workspace = nullptr;
-  {
-    std::lock_guard<std::mutex> lk(st->mu);
-    DeviceState::Workspace& w = st->workspaces[stream];
-    if (w.bytes < need) {
-      cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-      cudaError_t e = cudaStreamIsCapturing(stream, &cs);
-      if (e != cudaSuccess) return fail_cuda(e, "cudaStreamIsCapturing");
-      if (cs != cudaStreamCaptureStatusNone)
-        return fail(ATTN_ERR_NO_MEMORY,
-                    "decode workspace must grow but the stream is capturing; call once before "
-                    "capture with the largest shapes");
-      if (w.ptr) {
-        cudaStreamSynchronize(stream);
-        cudaFree(w.ptr);
-        w.ptr = nullptr;
-        w.bytes = 0;
-      }
-      void* ws = nullptr;
-      e = cudaMalloc(&ws, need);
-      if (e != cudaSuccess) {
-        cudaGetLastError();
-        return fail(ATTN_ERR_NO_MEMORY, std::string("workspace cudaMalloc: ") + cudaGetErrorString(e));
-      }
-      w.ptr = ws;
-      w.bytes = need;
-    }
-    workspace = w.ptr;
-  }
-
   const bool bf16 = dtype == ATTN_BF16;
   const int box_rows = paged ? (page_size < kt ? page_size : kt) : kt;
-  CUtensorMap mk, mv;
-  if (!decode_map(&mk, k_pool, paged ? num_pages : B, page_size, H_kv, D, box_rows, bf16) ||
-      !decode_map(&mv, v_pool, paged ? num_pages : B, page_size, H_kv, D, box_rows, bf16))
+  const int pages = paged ? num_pages : B;
+  if (!decode_map(&plan->mk, k_pool, pages, page_size, H_kv, D, box_rows, bf16) ||
+      !decode_map(&plan->mv, v_pool, pages, page_size, H_kv, D, box_rows, bf16))
     return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed for the KV pool");
 
-  attn_sm103a::DecodeParams p{};
+  // Partials: o_part [B, H_q, max_splits, D] then lse_part [B, H_q, max_splits].
+  const size_t rows = static_cast<size_t>(B) * H_q * max_splits;
+  plan->partial_bytes = rows * (D + 1) * sizeof(float);
+  plan->D = D;
+  plan->bf16 = bf16;
+  plan->o = o;
+  attn_sm103a::DecodeParams& p = plan->p;
   p.q = q;
   p.page_table = page_table;
   p.kv_lens = kv_lens;
-  p.o_part = static_cast<float*>(workspace);
-  p.lse_part = p.o_part + rows_ws * D;
   p.B = B;
   p.H_q = H_q;
   p.group = H_q / H_kv;
   p.page_size = page_size;
   p.max_pages = max_pages_per_seq;
-  p.num_pages = paged ? num_pages : B;
+  p.num_pages = pages;
   p.max_splits = max_splits;
   p.fixed_chunk = fixed_chunk;
   p.num_splits = num_splits > 0 ? num_splits : 1;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.err = st->err_word;
   p.wait_limit_ns = g_wait_limit_ns.load();
-  cudaError_t e = attn_sm103a::decode_launch(mk, mv, p, o, D, bf16, stream);
+  return ATTN_OK;
+}
+
+attn_status decode_enqueue(DecodePlan& plan, float* partials, cudaStream_t stream) {
+  const size_t rows = static_cast<size_t>(plan.p.B) * plan.p.H_q * plan.p.max_splits;
+  plan.p.o_part = partials;
+  plan.p.lse_part = partials + rows * plan.D;
+  cudaError_t e = attn_sm103a::decode_launch(plan.mk, plan.mv, plan.p, plan.o, plan.D,
+                                             plan.bf16, stream);
   if (e != cudaSuccess) return fail_cuda(e, "decode launch");
   return ATTN_OK;
 }
-
-attn_status attn_release_workspace(void) {
-  DeviceState* st = nullptr;
-  attn_status s = device_state(&st);
-  if (s != ATTN_OK) return s;
-  std::lock_guard<std::mutex> lk(st->mu);
-  if (!st->workspaces.empty()) {
-    cudaError_t e = cudaDeviceSynchronize();
-    if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceSynchronize");
-    for (auto& kv : st->workspaces) cudaFree(kv.second.ptr);
-    st->workspaces.clear();
-  }
-  if (!st->sched.empty()) {
-    cudaError_t e = cudaDeviceSynchronize();
-    if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceSynchronize");
-    for (auto& kv : st->sched) cudaFree(kv.second);
-    st->sched.clear();
-  }
-  return ATTN_OK;
-}
-
-}  // extern "C"
-
-// ------------------------------------------------------------------------
-// Internal accessors for other translation units of this library (the
-// allocation-free decode entry point).  They forward to the helpers above.
-namespace attn_internal {
-
-attn_status device_info(int** err_word, int* num_sms) {
-  DeviceState* st = nullptr;
-  attn_status s = device_state(&st);
-  if (s != ATTN_OK) return s;
-  *err_word = st->err_word;
-  *num_sms = st->num_sms;
-  return ATTN_OK;
-}
-
-attn_status set_error(attn_status s, const char* msg) { return fail(s, msg); }
-
-bool encode_decode_map(CUtensorMap* m, const void* base, int num_pages, int page_size, int H_kv,
-                       int D, int box_rows, bool bf16) {
-  return decode_map(m, base, num_pages, page_size, H_kv, D, box_rows, bf16);
-}
-
-uint64_t wait_limit_ns() { return g_wait_limit_ns.load(); }
-
-int split_chunk_override() { return env_int("ATTN_DECODE_SPLIT_CHUNK", 0); }
 
 }  // namespace attn_internal

@@ -32,6 +32,7 @@
 #include <type_traits>
 
 #include "backward_sm103a.h"
+#include "host_once.h"
 #include "sm103a_ptx.cuh"
 
 namespace attn_sm103a {
@@ -591,13 +592,12 @@ template <bool kBF16>
 cudaError_t launch_all(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                        const CUtensorMap& dout, const CUtensorMap& dq, const CUtensorMap& dk,
                        const CUtensorMap& dv, const BackwardParams& p, cudaStream_t stream) {
-  static bool configured = false;
-  if (!configured) {
+  static std::atomic<unsigned long long> configured{0};  // per template instance, per device
+  cudaError_t ce = attn_host::once_per_device(configured, [&]() {
     cudaError_t e = configure(bwd_dkdv_kernel<kBF16>);
-    if (e == cudaSuccess) e = configure(bwd_dq_kernel<kBF16>);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+    return e == cudaSuccess ? configure(bwd_dq_kernel<kBF16>) : e;
+  });
+  if (ce != cudaSuccess) return ce;
   const long long rows = static_cast<long long>(p.B) * p.H * p.S_q;
   if (rows > 0) {
     bwd_delta_kernel<kBF16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(p);

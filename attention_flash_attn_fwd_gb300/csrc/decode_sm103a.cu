@@ -27,6 +27,7 @@
 #include <cuda_fp16.h>
 
 #include "decode_sm103a.h"
+#include "host_once.h"
 #include "sm103a_ptx.cuh"
 
 namespace attn_sm103a {
@@ -378,13 +379,12 @@ template <int D, bool kBF16>
 cudaError_t launch_decode_t(const CUtensorMap& k, const CUtensorMap& v, const DecodeParams& p,
                             void* out, cudaStream_t stream) {
   auto kern = decode_split_kernel<D, kBF16>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         DCfg<D>::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<unsigned long long> configured{0};  // per template instance, per device
+  cudaError_t ce = attn_host::once_per_device(configured, [&]() {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                DCfg<D>::kSmemBytes);
+  });
+  if (ce != cudaSuccess) return ce;
   dim3 grid(p.max_splits, p.H_q / p.group, p.B);
   kern<<<grid, kThreads, DCfg<D>::kSmemBytes, stream>>>(k, v, p);
   cudaError_t e = cudaGetLastError();

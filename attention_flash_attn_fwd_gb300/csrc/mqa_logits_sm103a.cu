@@ -29,6 +29,7 @@
 // neither multiplied nor read back (the page's tile_skip / empty-window fix);
 // a tile no slab needs is not even loaded.  Every wait is bounded.
 #include "mqa_logits_sm103a.h"
+#include "host_once.h"
 #include "sm103a_ptx.cuh"
 
 #include <climits>
@@ -495,18 +496,17 @@ template <int H>
 cudaError_t launch_h(const CUtensorMap& q, const CUtensorMap& k, const MqaParams& p, dim3 grid,
                      cudaStream_t stream) {
   auto kern = mqa_logits_kernel<H>;
-  static bool configured = false;
-  if (!configured) {
+  static std::atomic<unsigned long long> configured{0};  // per template instance, per device
+  cudaError_t ce = attn_host::once_per_device(configured, [&]() {
     // The in-kernel register split assumes exactly kRegsLaunch registers per
     // thread at launch; with fewer, setmaxnreg.inc would never complete.
     cudaFuncAttributes fa{};
     cudaError_t e = cudaFuncGetAttributes(&fa, kern);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  });
+  if (ce != cudaSuccess) return ce;
   kern<<<grid, kThreads, kSmem, stream>>>(q, k, p);
   return cudaGetLastError();
 }

@@ -63,6 +63,8 @@
 // the per-tensor descale factors fold into the softmax scale and the final
 // 1/l.  O (bf16 or fp16) is staged in its own shared-memory tiles.
 #include "prefill_sm103a.h"
+
+#include "host_once.h"
 #include "sm103a_ptx.cuh"
 
 namespace attn_sm103a {
@@ -907,19 +909,18 @@ static cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const 
                               const CUtensorMap& o, const PrefillParams& p, int grid,
                               cudaStream_t stream) {
   auto kern = prefill_fwd_kernel<D, kBF16, kPaged, kFp8>;
-  static bool configured = false;  // per template instance
-  if (!configured) {
+  static std::atomic<unsigned long long> configured{0};  // per template instance, per device
+  cudaError_t ce = attn_host::once_per_device(configured, [&]() {
     // The in-kernel register split assumes exactly kRegsAtLaunch registers
     // per thread at launch; with fewer, setmaxnreg.inc would never complete.
     cudaFuncAttributes fa{};
     cudaError_t e = cudaFuncGetAttributes(&fa, kern);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != kRegsAtLaunch) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg<D, kFp8, kPaged>::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Cfg<D, kFp8, kPaged>::kSmemBytes);
+  });
+  if (ce != cudaSuccess) return ce;
   if (!(kPaged && p.pair)) {
     kern<<<grid, kThreads, Cfg<D, kFp8, kPaged>::kSmemBytes, stream>>>(q, k, v, o, p);
     return cudaGetLastError();

@@ -222,7 +222,8 @@ ATTN_API attn_status attn_extend_fwd(const void* q, const void* k_pool, const vo
  *   kv_lens    [B] int32 on the device, 0 <= kv_lens[b] <= max_pages_per_seq *
  *              page_size.  A sequence with kv_len 0 gets o = 0.
  *   o          [B,H_q,D] dtype output.
- *   page_size  keys per page (multiple of 8, <= 256 when paged).
+ *   page_size  keys per page: when paged, 8, 16, 32 or a multiple of 64 (else
+ *              ATTN_ERR_UNSUPPORTED); when contiguous, the capacity S_max (> 0).
  *   max_pages_per_seq  page_table row stride (ADDED to the published
  *              signature: the table's shape is not otherwise known); 1 when
  *              contiguous.
@@ -236,7 +237,11 @@ ATTN_API attn_status attn_extend_fwd(const void* q, const void* k_pool, const vo
  * The library owns a split-partials workspace per (device, stream), grown on
  * demand outside stream capture; growing it during capture returns
  * ATTN_ERR_NO_MEMORY (call once with the largest shapes, on the stream that
- * will be captured, before capturing).
+ * will be captured, before capturing).  A graph captured from a call keeps
+ * the workspace address of that call: a later call that has to grow the
+ * workspace retires the old buffer without freeing it, so such graphs stay
+ * valid until attn_release_workspace, which frees every buffer (after it,
+ * graphs captured earlier must not be replayed).
  * Calls on different streams may run concurrently; calls on one stream use
  * its workspace in stream order.
  */
@@ -247,22 +252,23 @@ ATTN_API attn_status attn_decode_fwd(const void* q, const void* k_pool, const vo
                             cudaStream_t stream);
 
 /*
- * Decode attention that allocates no device memory (no counterpart on the
- * source pages, which never discuss workspace ownership).
+ * Decode attention that allocates no device memory.  The source pages have no
+ * counterpart: they never discuss who owns a kernel's workspace.
  *
- * Same arguments, rules and results as attn_decode_fwd, for callers that must
- * not let a library allocate: code being captured into a CUDA graph, engines
- * whose framework owns all device memory through its own pool, and serving
- * loops that must not block on the allocator at step time.  The split
- * partials live in one fixed 16 MiB device array inside the library (held on
- * every GPU that loads it until the process exits) instead of a cudaMalloc'd
- * workspace; a call whose split plan needs more returns ATTN_ERR_UNSUPPORTED
- * and launches nothing (use num_splits > 0 with fewer splits, or
- * attn_decode_fwd).  The first call on a device looks up the array's device
- * address (cudaGetSymbolAddress); make that first call before any stream
- * capture.  All calls share the array and it keeps the last call's contents
- * (nothing in it needs to start at zero); calls whose kernels overlap on the
- * GPU race on it.
+ * Same arguments, rules and results as attn_decode_fwd (bitwise: the same
+ * checks, split plan and kernels), for callers that cannot let a library
+ * allocate: engines whose framework owns all device memory through its own
+ * pool and budget, and serving loops that must not block on the allocator or
+ * meet an out-of-memory error at step time.  The split partials live in one
+ * fixed 16 MiB device array inside the library (held on every GPU that loads
+ * it until the process exits) instead of a cudaMalloc'd workspace.  A call
+ * whose split plan needs more (B * H_q * splits * (D + 1) * 4 bytes) returns
+ * ATTN_ERR_UNSUPPORTED and launches nothing: pass num_splits > 0 with fewer
+ * splits, or use attn_decode_fwd.  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress); make that first call before
+ * any stream capture.  All calls share the array and it keeps the last call's
+ * contents (nothing in it needs to start at zero); calls whose kernels overlap
+ * on the GPU race on it.
  */
 ATTN_API attn_status attn_decode_fwd_noalloc(const void* q, const void* k_pool,
                                              const void* v_pool, const int32_t* page_table,
@@ -302,8 +308,10 @@ ATTN_API void attn_set_wait_limit_ns(uint64_t ns);
  */
 ATTN_API attn_status attn_selftest_wait_timeout(uint64_t limit_ns, cudaStream_t stream);
 
-/* Free the decode workspaces and prefill unit counters (all streams) of the
- * current device; synchronizes the device (not during capture). */
+/* Free the decode workspaces (current and retired) and prefill unit counters
+ * of all streams of the current device; synchronizes the device (not during
+ * capture).  CUDA graphs captured from earlier decode or prefill calls hold
+ * those addresses and must not be replayed after it. */
 ATTN_API attn_status attn_release_workspace(void);
 
 /* Library version string. */

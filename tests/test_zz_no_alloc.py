@@ -1,12 +1,15 @@
 """attn_decode_fwd_noalloc against attn_decode_fwd, through the C ABI.
 
 The allocation-free entry point serves callers that cannot let a library call
-cudaMalloc: code being captured into a CUDA graph, engines whose framework
-owns all device memory through its own pool, and serving loops that must not
-block on the allocator.  Its split partials live in a fixed device array
-inside the library instead of a grown workspace, so these tests check that it
-gives the allocating entry point's results, call after call, and that it
-refuses plans that do not fit the array.
+cudaMalloc: engines whose framework owns all device memory through its own
+pool and budget, and serving loops that must not block on the allocator or
+meet an out-of-memory error mid-step.  Its split partials live in a fixed
+device array inside the library instead of a grown workspace; the checks,
+split plan and kernels are the allocating entry point's own.  So these tests
+check that it gives the allocating entry point's results bit for bit (and so
+within the oracle tolerance the other tests use), on two calls in a row whose
+second call reuses the array the first one left behind, and that it refuses
+plans that do not fit the array.
 
 The file name makes pytest collect it last, so a failure here never hides the
 results of the other GPU tests; it also passes when run alone in a fresh
@@ -55,6 +58,8 @@ def test_noalloc_matches_allocating_decode_on_two_calls(paged, num_splits):
         torch.cuda.synchronize()
         assert attn.attn_device_error() == 0
         assert_close(got.cpu(), ref.double().cpu(), "noalloc vs decode (%s)" % case.name)
+        # Same checks, plan and kernels: any difference would be stale scratch.
+        assert torch.equal(got, ref), "noalloc differs from decode (%s)" % case.name
 
 
 def test_noalloc_rejects_plans_larger_than_its_array():
