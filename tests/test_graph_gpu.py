@@ -84,3 +84,33 @@ def test_mqa_logits_graph_replay():
     q8, kv8, sc, w, st, en = (t.cuda() for t in workloads.make_mqa(case))
     _graph_equals_eager(lambda: (attn.mqa_logits_fp8(q8, kv8, sc, w, st, en,
                                                      clean_logits=True),))
+
+
+def test_decode_graph_survives_workspace_growth():
+    """A decode call that has to grow its stream's workspace retires the old
+    buffer instead of freeing it, so a graph captured before the growth still
+    replays into valid memory and gives its eager bits."""
+    small = workloads.DecodeCase("g", 2, 8, 2, 128, 300, 600, 640, True, seed=57)
+    big = workloads.DecodeCase("g", 16, 32, 8, 128, 9000, 16000, 16384, True, seed=58)
+    s_in, b_in = workloads.make_decode(small), workloads.make_decode(big)
+    sd = [t.cuda() for t in (s_in.q, s_in.k, s_in.v, s_in.kv_lens, s_in.page_table)]
+    bd = [t.cuda() for t in (b_in.q, b_in.k, b_in.v, b_in.kv_lens, b_in.page_table)]
+    # Start from no workspace on any stream (no graph of an earlier test is
+    # replayed after this), so the small call sizes it and the big one grows it.
+    torch.cuda.synchronize()
+    assert attn.attn_release_workspace() == attn.ATTN_OK
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        eager = attn.decode(*sd[:4], page_table=sd[4]).clone()
+    side.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        static = attn.decode(*sd[:4], page_table=sd[4])
+    with torch.cuda.stream(side):  # needs a larger workspace on the same stream
+        big_out = attn.decode(*bd[:4], page_table=bd[4])
+    g.replay()
+    torch.cuda.synchronize()
+    assert attn.attn_device_error() == 0
+    assert torch.equal(static, eager)
+    assert torch.isfinite(big_out.float()).all()

@@ -89,16 +89,12 @@ def test_prefill_fp8_empty_kv_and_determinism():
 
 
 @pytest.mark.parametrize("case", [workloads.C7, workloads.C7_CAUSAL], ids=lambda c: c.name)
-def test_prefill_fp8_full_size_sampled_heads(case):
+def test_prefill_fp8_full_size(case):
+    """The measured FP8 workload at full size, every output element compared
+    with the oracle (persistent CTAs, many units each)."""
     inputs, o, lse = _run(case)
     q8, k8, v8, dq, dk, dv = inputs
-    g = torch.Generator().manual_seed(46)
-    for _ in range(3):
-        b = int(torch.randint(case.B, (1,), generator=g))
-        h = int(torch.randint(case.H, (1,), generator=g))
-        sl = lambda x: x[b:b + 1, h:h + 1]
-        ref_o, ref_lse = oracle.prefill_fp8(sl(q8), sl(k8), sl(v8), descale_q=dq, descale_k=dk,
-                                            descale_v=dv, causal=case.causal, scale=case.scale)
-        assert_close(o[b:b + 1, h:h + 1], ref_o, "%s b=%d h=%d" % (case.name, b, h), FP8_MAX_ABS,
-                     FP8_REL_L2)
-        assert_lse_close(lse[b:b + 1, h:h + 1], ref_lse, "%s lse" % case.name)
+    ref_o, ref_lse = oracle.prefill_fp8(q8, k8, v8, descale_q=dq, descale_k=dk, descale_v=dv,
+                                        causal=case.causal, scale=case.scale)
+    assert_close(o, ref_o, case.name, FP8_MAX_ABS, FP8_REL_L2)
+    assert_lse_close(lse, ref_lse, "%s lse" % case.name)

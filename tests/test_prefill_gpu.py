@@ -169,34 +169,21 @@ def test_layouts_agree_bitwise():
     assert torch.equal(o1, o2.transpose(1, 2))
 
 
-def _sampled_heads(case, heads):
-    """Run a full-size case on the GPU; check chosen (b, h) heads in full against the oracle."""
-    q, k, v = workloads.make_prefill(case)
-    o, lse = attn.prefill(q.cuda(), k.cuda(), v.cuda(), causal=case.causal, scale=case.scale,
-                          layout=case.layout, return_lse=True)
-    torch.cuda.synchronize()
-    assert attn.attn_device_error() == 0
-    o = o.cpu()
-    lse = lse.cpu()
-    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
-    for b, h in heads:
-        if case.layout == "bhsd":
-            sl = lambda x: x[b:b + 1, h:h + 1]  # noqa: E731
-        else:
-            sl = lambda x: x[b:b + 1, :, h:h + 1]  # noqa: E731
-        ref_o, ref_lse = oracle.prefill(sl(q), sl(k), sl(v), causal=case.causal, scale=case.scale,
-                                        layout=LAYOUT[case.layout])
-        assert_close(sl(o), ref_o, "%s b=%d h=%d" % (case.name, b, h))
-        assert_lse_close(lse[b:b + 1, h:h + 1], ref_lse, "%s lse" % case.name)
+# ------------------------------------------------------------ full size
+# The measured workloads, compared with the oracle over every output element
+# (no sampling).  Each launch runs persistent CTAs that take many units each
+# (C2: 2048 units, C3: 2560 units on 152 SMs), so the unit hand-over path (Q
+# refill, a K/V ring that continues across units, the O hand-off) is checked
+# on every head.  The oracle takes tens of seconds on the host cores here.
 
 
-def test_full_size_bhsd_fp16_noncausal_sampled():
-    _sampled_heads(workloads.C2, [(0, 0), (3, 31)])
+def test_full_size_bhsd_fp16_noncausal():
+    _check_full(workloads.C2)
 
 
-def test_full_size_bhsd_fp16_causal_sampled():
-    _sampled_heads(workloads.C2_CAUSAL, [(1, 7), (3, 30)])
+def test_full_size_bhsd_fp16_causal():
+    _check_full(workloads.C2_CAUSAL)
 
 
-def test_full_size_bshd_bf16_causal_sampled():
-    _sampled_heads(workloads.C3, [(0, 0), (7, 39), (4, 21)])
+def test_full_size_bshd_bf16_causal():
+    _check_full(workloads.C3)
