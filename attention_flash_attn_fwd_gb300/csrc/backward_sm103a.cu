@@ -63,6 +63,7 @@ struct BwdCtl {
   uint64_t full[kRing];       // walking pair (+ its lse/delta rows) has landed
   uint64_t empty[kRing];      // the MMAs reading a stage are done
   uint64_t mm_full;           // the two products of a step are in tensor memory
+  uint64_t p_ready;           // dK/dV kernel: P^T of a step is in tensor memory
   uint64_t ew_done;           // the element-wise pass of a step is in tensor memory
   uint64_t mma_done;          // every MMA of the CTA has completed
   uint64_t tmem_free;         // the element-wise warps are done with tensor memory
@@ -200,6 +201,58 @@ __device__ __forceinline__ void elementwise_step(uint32_t lane_addr, int g, uint
   tmem_st_wait();
 }
 
+// The dK/dV kernel's element-wise pass in two phases: P^T for all of the
+// warp's columns is stored and announced on `p_ready` first, so the MMA warp
+// runs dV += P^T dO while the warps compute dS^T = P^T (dP^T - delta).  Same
+// column ownership, barrier and arithmetic as elementwise_step.
+template <bool kBF16, bool kMasked, class Lse, class Delta, class Vis>
+__device__ __forceinline__ void elementwise_step_p_first(uint32_t lane_addr, int g, uint32_t cs,
+                                                         uint32_t cd, float c, int bar_id,
+                                                         Lse lse2_of, Delta delta_of,
+                                                         Vis visible, uint64_t* p_ready,
+                                                         int lane) {
+  uint32_t x[64], y[64];
+  tmem_ld64_wait(lane_addr + cs + 64 * g, x);
+  tmem_ld64_wait(lane_addr + cd + 64 * g, y);
+  named_barrier_sync(bar_id, kEwWarps * 32);
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    uint32_t pp[16];
+#pragma unroll
+    for (int q = 16 * hf; q < 16 * hf + 16; ++q) {
+      const int col0 = 64 * g + 2 * q;
+      const float2 l2 = lse2_of(col0);
+      float pv[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float pe = ex2_approx(fmaf(__uint_as_float(x[2 * q + e]), c, -(e ? l2.y : l2.x)));
+        if constexpr (kMasked) pe = visible(col0 + e) ? pe : 0.f;
+        pv[e] = pe;
+        x[2 * q + e] = __float_as_uint(pe);  // P in fp32 for the dS phase
+      }
+      pp[q - 16 * hf] = pack2<kBF16>(pv[0], pv[1]);
+    }
+    tmem_st16(lane_addr + cs + 32 * g + 16 * hf, pp);
+  }
+  tmem_st_wait();
+  tc_fence_before_sync();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(p_ready);
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    uint32_t dd[16];
+#pragma unroll
+    for (int q = 16 * hf; q < 16 * hf + 16; ++q) {
+      const float2 dl = delta_of(64 * g + 2 * q);
+      const float d0 = __uint_as_float(x[2 * q]) * (__uint_as_float(y[2 * q]) - dl.x);
+      const float d1 = __uint_as_float(x[2 * q + 1]) * (__uint_as_float(y[2 * q + 1]) - dl.y);
+      dd[q - 16 * hf] = pack2<kBF16>(d0, d1);
+    }
+    tmem_st16(lane_addr + cd + 32 * g + 16 * hf, dd);
+  }
+  tmem_st_wait();
+}
+
 // ---------------------------------------------------------------- delta
 
 // delta[b,h,i] = sum_d dO[b,h,i,d] * O[b,h,i,d] in fp32; one warp per row.
@@ -269,6 +322,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       mbar_init(&ctl->empty[s], 1);
     }
     mbar_init(&ctl->mm_full, 1);
+    mbar_init(&ctl->p_ready, kEwWarps);
     mbar_init(&ctl->ew_done, kEwWarps);
     mbar_init(&ctl->mma_done, 1);
     mbar_init(&ctl->tmem_free, kEwWarps);
@@ -356,10 +410,13 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         mma_abt(tmem + 0, k_lo, sdesc_lo(stage, 16), hi, id_s);            // S^T = K Q^T
         mma_abt(tmem + 128, v_lo, sdesc_lo(stage + kTile, 16), hi, id_s);  // dP^T = V dO^T
         mma_commit(&ctl->mm_full);
+        // dV += P^T dO as soon as P^T is in place (while dS^T is computed),
+        // then dK += dS^T Q; the walking tiles are read MN-major.
+        if (!(ok = mbar_wait(&ctl->p_ready, s & 1, p.wait_limit_ns, p.err, 68))) break;
+        tc_fence_after_sync();
+        mma_tmem_a(tmem + 256, tmem + 0, sdesc_lo(stage + kTile, kPanel), hi, id_o, s > 0);
         if (!(ok = mbar_wait(&ctl->ew_done, s & 1, p.wait_limit_ns, p.err, 65))) break;
         tc_fence_after_sync();
-        // dV += P^T dO and dK += dS^T Q, the walking tiles read MN-major
-        mma_tmem_a(tmem + 256, tmem + 0, sdesc_lo(stage + kTile, kPanel), hi, id_o, s > 0);
         mma_tmem_a(tmem + 384, tmem + 128, sdesc_lo(stage, kPanel), hi, id_o, s > 0);
         mma_commit(&ctl->empty[st]);
       }
@@ -390,14 +447,18 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       const int q0 = (first + s) * kT;
       const bool full = key0 + kT <= p.S_kv && q0 + kT <= p.S_q &&
                         (!p.causal || key0 + kT - 1 <= q0 + off);
-      elementwise_step<kBF16>(
-          lane_addr, g, 0, 128, p.scale_log2, !full, 2,
-          [=](int col) { return *reinterpret_cast<const float2*>(lse2 + col); },
-          [=](int col) { return *reinterpret_cast<const float2*>(dlt + col); },
-          [=](int col) {
-            const int i = q0 + col;
-            return key < p.S_kv && i < p.S_q && (!p.causal || key <= i + off);
-          });
+      auto lse2_of = [=](int col) { return *reinterpret_cast<const float2*>(lse2 + col); };
+      auto delta_of = [=](int col) { return *reinterpret_cast<const float2*>(dlt + col); };
+      auto visible = [=](int col) {
+        const int i = q0 + col;
+        return key < p.S_kv && i < p.S_q && (!p.causal || key <= i + off);
+      };
+      if (full)
+        elementwise_step_p_first<kBF16, false>(lane_addr, g, 0, 128, p.scale_log2, 2, lse2_of,
+                                               delta_of, visible, &ctl->p_ready, lane);
+      else
+        elementwise_step_p_first<kBF16, true>(lane_addr, g, 0, 128, p.scale_log2, 2, lse2_of,
+                                              delta_of, visible, &ctl->p_ready, lane);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->ew_done);
@@ -468,6 +529,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       mbar_init(&ctl->empty[s], 1);
     }
     mbar_init(&ctl->mm_full, 1);
+    mbar_init(&ctl->p_ready, kEwWarps);
     mbar_init(&ctl->ew_done, kEwWarps);
     mbar_init(&ctl->mma_done, 1);
     mbar_init(&ctl->tmem_free, kEwWarps);
