@@ -18,14 +18,17 @@
 //    dK += dS^T Q read P^T / dS^T straight from tensor memory.  Tensor memory:
 //    S^T [0,128), dP^T [128,256), dV [256,384), dK [384,512).
 //  * dQ: a CTA owns 128 queries (Q, dO resident) and walks the key tiles they
-//    see: S = Q K^T, dP = dO V^T, P and dS in place, dQ += dS K.  Tensor
-//    memory: S [0,128), dP [128,256) (dS in its first half), dQ [256,384).
+//    see: S = Q K^T, dP = dO V^T, dS, dQ += dS K.  Tensor memory: S [0,128),
+//    dP [128,256), dQ [256,384), dS [384,448).  Pipelined: once the
+//    element-wise warps hold a step's S and dP in registers, the next step's
+//    products overwrite them while dS is computed; K and V stream through
+//    rings of their own (3 and 2 stages).
 // The dQ pass recomputes S and dP (7 MMAs per tile pair instead of 5) so that
 // no tile's gradient needs atomic accumulation: results are deterministic.
-// A TMA warp streams the walking tiles through a 2-stage ring, an MMA warp
-// issues tcgen05.mma, eight warps do the element-wise work (two warpgroups,
-// each taking 64 of the 128 columns of every row); every wait is bounded in
-// time.
+// A TMA warp streams the walking tiles (dK/dV: a 2-stage ring of (Q, dO)
+// pairs), an MMA warp issues tcgen05.mma, eight warps do the element-wise
+// work (two warpgroups, each taking 64 of the 128 columns of every row);
+// every wait is bounded in time.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -493,6 +496,40 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 
 // ---------------------------------------------------------------- dQ
 
+// The dQ kernel streams K and V through rings of their own: V_j is read only
+// by dP_j and is released early; K_j is read by S_j and, one step later in
+// the pipeline below, by dQ += dS_j K_j.  Three K stages and two V stages of
+// 32 KB fit beside the resident Q and dO.
+constexpr int kKStages = 3;
+constexpr int kVStages = 2;
+constexpr int kOffDqK = 2 * kTile;
+constexpr int kOffDqV = kOffDqK + kKStages * kTile;
+constexpr int kOffDqCtl = kOffDqV + kVStages * kTile;
+constexpr int kSmemDq = kOffDqCtl + 256 + 1024;
+
+struct DqCtl {
+  uint64_t res_full;            // the resident Q and dO have landed
+  uint64_t k_full[kKStages];    // K_j has landed
+  uint64_t k_empty[kKStages];   // S_j and dQ_j have read K_j
+  uint64_t v_full[kVStages];
+  uint64_t v_empty[kVStages];   // dP_j has read V_j
+  uint64_t mm_full;             // S_j and dP_j are in tensor memory
+  uint64_t loaded;              // the element-wise warps hold S_j and dP_j in registers
+  uint64_t ew_done;             // dS_j is in tensor memory (columns [384, 448))
+  uint64_t ds_free;             // dQ_{j-1} has read the dS columns
+  uint64_t mma_done;            // every MMA of the CTA has completed
+  uint64_t tmem_free;           // the element-wise warps are done with tensor memory
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(DqCtl) <= 256, "control block must fit its reserved bytes");
+static_assert(kSmemDq <= 232448, "dQ shared memory exceeds the per-block limit");
+
+// Pipelined per key tile j: S_j = Q K_j^T and dP_j = dO V_j^T into tensor
+// memory [0, 256); the element-wise warps load both into registers and
+// announce it, so the MMA warp issues S_{j+1}, dP_{j+1} over them while dS_j
+// is computed and stored in columns [384, 448) of its own; then dQ += dS_j K_j
+// into [256, 384).
 template <bool kBF16>
 __global__ void __launch_bounds__(kThreadsB, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -505,7 +542,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* s_q = smem;
   uint8_t* s_do = smem + kTile;
-  BwdCtl* ctl = reinterpret_cast<BwdCtl*>(smem + kOffCtl);
+  uint8_t* s_k = smem + kOffDqK;  // kKStages tiles
+  uint8_t* s_v = smem + kOffDqV;  // kVStages tiles
+  DqCtl* ctl = reinterpret_cast<DqCtl*>(smem + kOffDqCtl);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
   const int nqt = (p.S_q + kT - 1) / kT;
@@ -524,13 +563,18 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   }
   if (threadIdx.x == 0) {
     mbar_init(&ctl->res_full, 1);
-    for (int s = 0; s < kRing; ++s) {
-      mbar_init(&ctl->full[s], 1);
-      mbar_init(&ctl->empty[s], 1);
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(&ctl->k_full[s], 1);
+      mbar_init(&ctl->k_empty[s], 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(&ctl->v_full[s], 1);
+      mbar_init(&ctl->v_empty[s], 1);
     }
     mbar_init(&ctl->mm_full, 1);
-    mbar_init(&ctl->p_ready, kEwWarps);
+    mbar_init(&ctl->loaded, kEwWarps);
     mbar_init(&ctl->ew_done, kEwWarps);
+    mbar_init(&ctl->ds_free, 1);
     mbar_init(&ctl->mma_done, 1);
     mbar_init(&ctl->tmem_free, kEwWarps);
     ctl->abort = 0;
@@ -545,50 +589,76 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   if (warp >= kEwWarps) {
    setmaxnreg_dec<kRegsCtl>();
    if (warp == kWarpLoad) {
+    // ---------------------------------------------------------- producer
     if (lane == 0 && n_steps > 0) {
       mbar_arrive_expect_tx(&ctl->res_full, 2 * kTile);
       load_tile(s_q, &tm_q, &ctl->res_full, q0, h, b, p.bshd);
       load_tile(s_do, &tm_do, &ctl->res_full, q0, h, b, p.bshd);
-      int issued = 0;
+      int issued = 0, v_issued = 0;  // K and V tiles whose copies were issued
       for (int s = 0; s < n_steps && !*abort_flag; ++s) {
-        const int st = s % kRing;
-        if (s >= kRing &&
-            !mbar_wait(&ctl->empty[st], (s / kRing - 1) & 1, p.wait_limit_ns, p.err, 80)) {
+        const int sk = s % kKStages, sv = s % kVStages;
+        if (s >= kKStages &&
+            !mbar_wait(&ctl->k_empty[sk], (s / kKStages - 1) & 1, p.wait_limit_ns, p.err, 80)) {
           *abort_flag = 1;
           break;
         }
-        uint8_t* stage = smem + kOffRing + st * 2 * kTile;
-        mbar_arrive_expect_tx(&ctl->full[st], 2 * kTile);
-        load_tile(stage, &tm_k, &ctl->full[st], s * kT, h, b, p.bshd);
-        load_tile(stage + kTile, &tm_v, &ctl->full[st], s * kT, h, b, p.bshd);
-        issued = s + 1;
+        mbar_arrive_expect_tx(&ctl->k_full[sk], kTile);
+        load_tile(s_k + sk * kTile, &tm_k, &ctl->k_full[sk], s * kT, h, b, p.bshd);
+        issued = s + 1;  // K_s is in flight from here on
+        if (s >= kVStages &&
+            !mbar_wait(&ctl->v_empty[sv], (s / kVStages - 1) & 1, p.wait_limit_ns, p.err, 79)) {
+          *abort_flag = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(&ctl->v_full[sv], kTile);
+        load_tile(s_v + sv * kTile, &tm_v, &ctl->v_full[sv], s * kT, h, b, p.bshd);
+        v_issued = s + 1;
       }
-      for (int s = max(0, issued - kRing); s < issued; ++s)
-        mbar_wait(&ctl->full[s % kRing], (s / kRing) & 1, p.wait_limit_ns, p.err, 81);
+      // No copy may still be landing when the CTA exits: wait (bounded) for
+      // the last load issued into every stage.
+      for (int s = max(0, issued - kKStages); s < issued; ++s)
+        mbar_wait(&ctl->k_full[s % kKStages], (s / kKStages) & 1, p.wait_limit_ns, p.err, 81);
+      for (int s = max(0, v_issued - kVStages); s < v_issued; ++s)
+        mbar_wait(&ctl->v_full[s % kVStages], (s / kVStages) & 1, p.wait_limit_ns, p.err, 78);
       mbar_wait(&ctl->res_full, 0, p.wait_limit_ns, p.err, 82);
     }
     __syncwarp();
    } else if (warp == kWarpMmaB) {
+    // ---------------------------------------------------------- MMA issuer
     if (lane == 0 && n_steps > 0) {
       constexpr uint32_t id_s = idesc_f16(kBF16, kT, kT, false, false);
       constexpr uint32_t id_o = idesc_f16(kBF16, kT, kT, false, true);
       const uint32_t hi = sdesc_hi_sw128(1024);
       const uint32_t q_lo = sdesc_lo(smem_u32(s_q), 16);
       const uint32_t do_lo = sdesc_lo(smem_u32(s_do), 16);
-      bool ok = mbar_wait(&ctl->res_full, 0, p.wait_limit_ns, p.err, 83);
-      for (int s = 0; s < n_steps && ok; ++s) {
-        const int st = s % kRing;
-        const uint32_t stage = smem_u32(smem + kOffRing + st * 2 * kTile);
-        if (!(ok = mbar_wait(&ctl->full[st], (s / kRing) & 1, p.wait_limit_ns, p.err, 84))) break;
+      // S_s = Q K_s^T and dP_s = dO V_s^T; V_s is released right after.
+      auto products = [&](int s) {
+        const int sk = s % kKStages, sv = s % kVStages;
+        if (!mbar_wait(&ctl->k_full[sk], (s / kKStages) & 1, p.wait_limit_ns, p.err, 84) ||
+            !mbar_wait(&ctl->v_full[sv], (s / kVStages) & 1, p.wait_limit_ns, p.err, 89))
+          return false;
         tc_fence_after_sync();
-        mma_abt(tmem + 0, q_lo, sdesc_lo(stage, 16), hi, id_s);            // S = Q K^T
-        mma_abt(tmem + 128, do_lo, sdesc_lo(stage + kTile, 16), hi, id_s);  // dP = dO V^T
+        mma_abt(tmem + 0, q_lo, sdesc_lo(smem_u32(s_k + sk * kTile), 16), hi, id_s);
+        mma_abt(tmem + 128, do_lo, sdesc_lo(smem_u32(s_v + sv * kTile), 16), hi, id_s);
         mma_commit(&ctl->mm_full);
+        mma_commit(&ctl->v_empty[sv]);
+        return true;
+      };
+      bool ok = mbar_wait(&ctl->res_full, 0, p.wait_limit_ns, p.err, 83);
+      if (ok) ok = products(0);
+      for (int s = 0; s < n_steps && ok; ++s) {
+        if (s + 1 < n_steps) {
+          if (!(ok = mbar_wait(&ctl->loaded, s & 1, p.wait_limit_ns, p.err, 88))) break;
+          if (!(ok = products(s + 1))) break;
+        }
         if (!(ok = mbar_wait(&ctl->ew_done, s & 1, p.wait_limit_ns, p.err, 85))) break;
         tc_fence_after_sync();
-        // dQ += dS K (dS in columns [128, 192)), K read MN-major
-        mma_tmem_a(tmem + 256, tmem + 128, sdesc_lo(stage, kPanel), hi, id_o, s > 0);
-        mma_commit(&ctl->empty[st]);
+        // dQ += dS_s K_s (dS in columns [384, 448)), K read MN-major
+        const int sk = s % kKStages;
+        mma_tmem_a(tmem + 256, tmem + 384, sdesc_lo(smem_u32(s_k + sk * kTile), kPanel), hi, id_o,
+                   s > 0);
+        mma_commit(&ctl->ds_free);
+        mma_commit(&ctl->k_empty[sk]);
       }
       if (!ok) *abort_flag = 1;
       mma_commit(&ctl->mma_done);
@@ -601,6 +671,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
    }
   } else {
     setmaxnreg_inc<kRegsEw>();
+    // ---------------------------------------------------------- element-wise
     const int g = warp / 4;                // column group of this warp
     const int r = (warp % 4) * 32 + lane;  // query row within the tile
     const int i = q0 + r;
@@ -608,22 +679,46 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     const size_t ridx = static_cast<size_t>(bh) * p.S_q + i;
     const float lse2 = i < p.S_q ? p.lse[ridx] * kLog2e : 0.f;
     const float dlt = i < p.S_q ? p.delta[ridx] : 0.f;
+    const float c = p.scale_log2;
     bool ok = true;
     for (int s = 0; s < n_steps; ++s) {
       ok = __all_sync(0xffffffffu, mbar_wait(&ctl->mm_full, s & 1, p.wait_limit_ns, p.err, 90));
       if (!ok) break;
       tc_fence_after_sync();
+      uint32_t x[64], y[64];
+      tmem_ld64_wait(lane_addr + 0 + 64 * g, x);    // S, this warp's 64 key columns
+      tmem_ld64_wait(lane_addr + 128 + 64 * g, y);  // dP
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->loaded);  // the MMA warp may overwrite S and dP
       const int k0 = s * kT;
       const bool full = k0 + kT <= p.S_kv && q0 + kT <= p.S_q &&
                         (!p.causal || k0 + kT - 1 <= q0 + off);
-      elementwise_step<kBF16>(
-          lane_addr, g, 0, 128, p.scale_log2, !full, 2,
-          [=](int) { return make_float2(lse2, lse2); },
-          [=](int) { return make_float2(dlt, dlt); },
-          [=](int col) {
-            const int key = k0 + col;
-            return key < p.S_kv && i < p.S_q && (!p.causal || key <= i + off);
-          });
+      uint32_t dd[32];  // dS as 16-bit pairs: column 32g + q holds keys 64g + 2q, + 1
+#pragma unroll
+      for (int q = 0; q < 32; ++q) {
+        float dv[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float pe = ex2_approx(fmaf(__uint_as_float(x[2 * q + e]), c, -lse2));
+          if (!full) {
+            const int key = k0 + 64 * g + 2 * q + e;
+            pe = (key < p.S_kv && i < p.S_q && (!p.causal || key <= i + off)) ? pe : 0.f;
+          }
+          dv[e] = pe * (__uint_as_float(y[2 * q + e]) - dlt);
+        }
+        dd[q] = pack2<kBF16>(dv[0], dv[1]);
+      }
+      // dQ_{s-1} must have read the dS columns before they are overwritten.
+      if (s > 0) {
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(&ctl->ds_free, (s - 1) & 1, p.wait_limit_ns, p.err, 92));
+        if (!ok) break;
+        tc_fence_after_sync();
+      }
+      tmem_st16(lane_addr + 384 + 32 * g, *reinterpret_cast<uint32_t(*)[16]>(dd));
+      tmem_st16(lane_addr + 384 + 32 * g + 16, *reinterpret_cast<uint32_t(*)[16]>(dd + 16));
+      tmem_st_wait();
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->ew_done);
@@ -652,14 +747,14 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 }
 
 template <class K>
-cudaError_t configure(K kern) {
+cudaError_t configure(K kern, int smem_bytes) {
   // The in-kernel register split assumes exactly kRegsLaunchB registers per
   // thread at launch; with fewer, setmaxnreg.inc would never complete.
   cudaFuncAttributes fa{};
   cudaError_t e = cudaFuncGetAttributes(&fa, kern);
   if (e != cudaSuccess) return e;
   if (fa.numRegs != kRegsLaunchB) return cudaErrorInvalidConfiguration;
-  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemB);
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
 }
 
 template <bool kBF16>
@@ -668,8 +763,8 @@ cudaError_t launch_all(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
                        const CUtensorMap& dv, const BackwardParams& p, cudaStream_t stream) {
   static std::atomic<unsigned long long> configured{0};  // per template instance, per device
   cudaError_t ce = attn_host::once_per_device(configured, [&]() {
-    cudaError_t e = configure(bwd_dkdv_kernel<kBF16>);
-    return e == cudaSuccess ? configure(bwd_dq_kernel<kBF16>) : e;
+    cudaError_t e = configure(bwd_dkdv_kernel<kBF16>, kSmemB);
+    return e == cudaSuccess ? configure(bwd_dq_kernel<kBF16>, kSmemDq) : e;
   });
   if (ce != cudaSuccess) return ce;
   const long long rows = static_cast<long long>(p.B) * p.H * p.S_q;
@@ -686,7 +781,7 @@ cudaError_t launch_all(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (p.B * p.H * nqt > 0)
-    bwd_dq_kernel<kBF16><<<p.B * p.H * nqt, kThreadsB, kSmemB, stream>>>(q, k, v, dout, dq, p);
+    bwd_dq_kernel<kBF16><<<p.B * p.H * nqt, kThreadsB, kSmemDq, stream>>>(q, k, v, dout, dq, p);
   return cudaGetLastError();
 }
 
