@@ -218,6 +218,8 @@ __device__ __forceinline__ void elementwise_step_p_first(uint32_t lane_addr, int
   tmem_ld64_wait(lane_addr + cs + 64 * g, x);
   tmem_ld64_wait(lane_addr + cd + 64 * g, y);
   named_barrier_sync(bar_id, kEwWarps * 32);
+  // Column pairs in packed fp32 (f32x2): one instruction per two elements.
+  const uint64_t c2 = f2_pack(c, c);
 #pragma unroll
   for (int hf = 0; hf < 2; ++hf) {
     uint32_t pp[16];
@@ -225,15 +227,18 @@ __device__ __forceinline__ void elementwise_step_p_first(uint32_t lane_addr, int
     for (int q = 16 * hf; q < 16 * hf + 16; ++q) {
       const int col0 = 64 * g + 2 * q;
       const float2 l2 = lse2_of(col0);
-      float pv[2];
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        float pe = ex2_approx(fmaf(__uint_as_float(x[2 * q + e]), c, -(e ? l2.y : l2.x)));
-        if constexpr (kMasked) pe = visible(col0 + e) ? pe : 0.f;
-        pv[e] = pe;
-        x[2 * q + e] = __float_as_uint(pe);  // P in fp32 for the dS phase
+      float a0, a1;
+      f2_unpack(f2_fma(f2_pack(__uint_as_float(x[2 * q]), __uint_as_float(x[2 * q + 1])), c2,
+                       f2_pack(-l2.x, -l2.y)),
+                a0, a1);
+      float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+      if constexpr (kMasked) {
+        p0 = visible(col0) ? p0 : 0.f;
+        p1 = visible(col0 + 1) ? p1 : 0.f;
       }
-      pp[q - 16 * hf] = pack2<kBF16>(pv[0], pv[1]);
+      x[2 * q] = __float_as_uint(p0);  // P in fp32 for the dS phase
+      x[2 * q + 1] = __float_as_uint(p1);
+      pp[q - 16 * hf] = pack2<kBF16>(p0, p1);
     }
     tmem_st16(lane_addr + cs + 32 * g + 16 * hf, pp);
   }
@@ -247,8 +252,13 @@ __device__ __forceinline__ void elementwise_step_p_first(uint32_t lane_addr, int
 #pragma unroll
     for (int q = 16 * hf; q < 16 * hf + 16; ++q) {
       const float2 dl = delta_of(64 * g + 2 * q);
-      const float d0 = __uint_as_float(x[2 * q]) * (__uint_as_float(y[2 * q]) - dl.x);
-      const float d1 = __uint_as_float(x[2 * q + 1]) * (__uint_as_float(y[2 * q + 1]) - dl.y);
+      // dS = P (dP - delta), as (dP - delta) then P * that, both packed
+      const uint64_t t = f2_add(f2_pack(__uint_as_float(y[2 * q]), __uint_as_float(y[2 * q + 1])),
+                                f2_pack(-dl.x, -dl.y));
+      float d0, d1;
+      f2_unpack(f2_fma(f2_pack(__uint_as_float(x[2 * q]), __uint_as_float(x[2 * q + 1])), t,
+                       f2_pack(0.f, 0.f)),
+                d0, d1);
       dd[q - 16 * hf] = pack2<kBF16>(d0, d1);
     }
     tmem_st16(lane_addr + cd + 32 * g + 16 * hf, dd);
@@ -695,19 +705,27 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       const bool full = k0 + kT <= p.S_kv && q0 + kT <= p.S_q &&
                         (!p.causal || k0 + kT - 1 <= q0 + off);
       uint32_t dd[32];  // dS as 16-bit pairs: column 32g + q holds keys 64g + 2q, + 1
+      // Column pairs in packed fp32 (f32x2): one instruction per two elements.
+      const uint64_t c2 = f2_pack(c, c), nl2 = f2_pack(-lse2, -lse2);
+      const uint64_t nd2 = f2_pack(-dlt, -dlt), z2 = f2_pack(0.f, 0.f);
 #pragma unroll
       for (int q = 0; q < 32; ++q) {
-        float dv[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          float pe = ex2_approx(fmaf(__uint_as_float(x[2 * q + e]), c, -lse2));
-          if (!full) {
-            const int key = k0 + 64 * g + 2 * q + e;
-            pe = (key < p.S_kv && i < p.S_q && (!p.causal || key <= i + off)) ? pe : 0.f;
-          }
-          dv[e] = pe * (__uint_as_float(y[2 * q + e]) - dlt);
+        float a0, a1;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(x[2 * q]), __uint_as_float(x[2 * q + 1])), c2,
+                         nl2),
+                  a0, a1);
+        float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+        if (!full) {
+          const int key = k0 + 64 * g + 2 * q;
+          const bool row_ok = i < p.S_q;
+          p0 = (row_ok && key < p.S_kv && (!p.causal || key <= i + off)) ? p0 : 0.f;
+          p1 = (row_ok && key + 1 < p.S_kv && (!p.causal || key + 1 <= i + off)) ? p1 : 0.f;
         }
-        dd[q] = pack2<kBF16>(dv[0], dv[1]);
+        const uint64_t t =
+            f2_add(f2_pack(__uint_as_float(y[2 * q]), __uint_as_float(y[2 * q + 1])), nd2);
+        float d0, d1;
+        f2_unpack(f2_fma(f2_pack(p0, p1), t, z2), d0, d1);
+        dd[q] = pack2<kBF16>(d0, d1);
       }
       // dQ_{s-1} must have read the dS columns before they are overwritten.
       if (s > 0) {
