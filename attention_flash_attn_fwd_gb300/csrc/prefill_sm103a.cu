@@ -433,9 +433,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // A unit is taken only when the previous one is fully issued, so
       // faster CTAs take more of the (unequal, causal) units.
+      // Causal units have unequal lengths.  Head-major order (unit_info)
+      // keeps the units in flight on a few heads, whose K/V stay in L2, but
+      // the last heads' long units would start late and leave the other CTAs
+      // idle at the end; so the last ~2 waves' worth of heads (their K/V
+      // still fit in L2) hand out their units longest first across heads.
+      // The producer maps the n-th unit taken to its head-major index once;
+      // every role then decodes that index with unit_info.
+      const int nbh = p.B * p.H;
+      const int tail_bh = p.causal ? min(nbh, (2 * p.ctas + nqb - 1) / nqb) : 0;
+      const int u_tail = (nbh - tail_bh) * nqb;
+      auto head_major = [&](int u) {
+        if (u < u_tail) return u;
+        const int v = u - u_tail;
+        return (nbh - tail_bh + v % tail_bh) * nqb + v / tail_bh;
+      };
       for (int n = 0; ok; ++n) {
         int u = dyn ? atomicAdd(p.sched, 1) : (n == 0 ? static_cast<int>(blockIdx.x) : n_units);
-        if (u >= n_units || *abort_flag) u = -1;
+        u = (u >= n_units || *abort_flag) ? -1 : head_major(u);
         const int slot = n & 1;
         if (n >= 2 &&
             !(ok = mbar_wait(&ctl->unit_empty[slot], ((n >> 1) - 1) & 1, p.wait_limit_ns, p.err,
