@@ -117,7 +117,7 @@ struct SharedCtl {
   uint64_t q_empty[kTiles];    // the unit's last S MMA of tile t has read Q_t
   uint64_t s_full[kTiles];
   uint64_t p_full[kTiles];     // P_t (all 128 keys) is in tensor memory
-  uint64_t o_full[kTiles];     // the unit's last PV MMA of tile t is done
+  uint64_t o_full[kTiles];     // the unit's last PV MMA of tile t is done (tiles with keys)
   uint64_t o_free[kTiles];     // the softmax warps of tile t hold O_t in registers
   uint64_t unit_full[2];       // a unit id was published in unit_ring
   uint64_t unit_empty[2];      // the MMA warp and every softmax warp read it
@@ -563,8 +563,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&ctl->unit_empty[n & 1]);
         if (u < 0) break;
         const Unit U = unit_info(u);
-        // Each query tile releases its Q (q_empty) after its last S MMA and
-        // signals its O (o_full) after its last PV MMA, exactly once per unit.
+        // Each query tile releases its Q (q_empty) after its last S MMA,
+        // exactly once per unit, and signals its O (o_full) after its last PV
+        // MMA, once per unit in which it has keys.  (A unit without keys
+        // signalling o_full at once could complete two phases before a
+        // waiter still on the previous unit looked, which it would then
+        // never see.)
         if (U.n_all > 0 && !(ok = wait_full(base, 21))) break;
         for (int t = 0; t < kTiles && ok; ++t) {
           if (!(ok = mbar_wait(&ctl->q_full[t], n & 1, p.wait_limit_ns, p.err, 20))) break;
@@ -574,7 +578,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(&ctl->s_full[t]);
           }
           if (U.n_kv(t) <= 1) mma_commit(&ctl->q_empty[t]);
-          if (U.n_kv(t) == 0) mma_commit(&ctl->o_full[t]);
         }
         if (!ok) break;
         if (U.n_all > 0) release(base % C::kStages);
@@ -640,7 +643,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t col_s = C::col_s(t);
     const uint32_t col_o = C::col_o(t);
     const float c = p.scale_log2;
-    int ns = 0;  // S tiles of this query tile consumed, all units
+    int ns = 0;   // S tiles of this query tile consumed, all units
+    int nof = 0;  // O tiles of this query tile with keys consumed, all units
     bool ok = true;
     for (int n = 0; ok; ++n) {
       ok = __all_sync(0xffffffffu, mbar_wait(&ctl->unit_full[n & 1], (n >> 1) & 1,
@@ -766,15 +770,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
 
       // ---------------------------------------------------------- epilogue
-      ok = __all_sync(0xffffffffu,
-                      mbar_wait(&ctl->o_full[t], n & 1, p.wait_limit_ns, p.err, 40 + t));
-      if (!ok) break;
-      tc_fence_after_sync();
+      if (n_kv > 0) {
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(&ctl->o_full[t], nof & 1, p.wait_limit_ns, p.err, 40 + t));
+        if (!ok) break;
+        ++nof;
+        tc_fence_after_sync();
+      }
       const bool have_o = n_kv > 0 && l > 0.f;
       const float inv_l = have_o ? p.o_scale / l : 0.f;
       if constexpr (kPaged) {
-        // One unit per CTA: Q_t is dead and holds O_t for a TMA store.
+        // One unit per CTA: Q_t is dead and holds O_t for a TMA store.  With
+        // keys, the last PV MMA (o_full) followed every read of Q_t; without,
+        // only Q_t's own load may still be landing there.
         uint8_t* s_o = s_q + t * C::kTileBytes;
+        if (n_kv == 0) {
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(&ctl->q_full[t], 0, p.wait_limit_ns, p.err, 39));
+          if (!ok) break;
+        }
 #pragma unroll 1
         for (int cc = 0; cc < D; cc += 64) {
           uint32_t o[64] = {};
