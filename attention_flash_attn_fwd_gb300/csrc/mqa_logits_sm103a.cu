@@ -18,14 +18,15 @@
 // epilogue warpgroups take the (tile, slab) units round-robin, so the MMA runs
 // ahead while a sub-partition's three epilogue warps hide each other's loads.
 //
-// Epilogue: each warp reads its 32 keys of a buffer as two 16x256b loads, so
-// a thread holds 4 keys x 32 of the slab's 128 columns and every weight it
-// reads from shared memory serves 4 keys.  The ReLU is split across two pipes
-// (an integer max on the ALU for one key of a register pair, an exact
-// saturating multiply on the FMA pipe for the other; see KeyScale), the
-// weighted sum is a packed FMA, and two shuffle steps finish the head sum
-// across the 4 threads that share a key.  Stores run along the key axis (128 contiguous bytes per row and
-// warp).  A (tile, slab) pair none of whose rows' windows meets the tile is
+// Epilogue: each thread owns one key (its tensor-memory lane) and reads all
+// 128 of the slab's columns as two 64-column loads, so the weighted head sum
+// stays inside the thread, and every weight load is a 16-byte broadcast
+// serving 4 columns.  For keys with a non-negative scale the ReLU needs no
+// scale at all (it factors out of the head sum) and is split across two
+// pipes (an integer max on the ALU for half of the columns, an exact
+// saturating multiply on the FMA pipe for the other half; see
+// accumulate64); the weighted sum is a packed FMA.  Stores run along the key
+// axis (128 contiguous bytes per row and warp).  A (tile, slab) pair none of whose rows' windows meets the tile is
 // neither multiplied nor read back (the page's tile_skip / empty-window fix);
 // a tile no slab needs is not even loaded.  Every wait is bounded.
 #include "mqa_logits_sm103a.h"
@@ -93,80 +94,72 @@ __device__ __forceinline__ bool slab_live(int slo, int shi, int key0) {
   return slo < key0 + kKeys && shi > key0;
 }
 
-// ReLU by saturation.  For E4M3 operands |q.k| <= 128 * 448^2 < 2^25, so with
-// |scale| <= 2^e the product x * scale * 2^-(25+e) lies in [-1, 1] and a
-// saturating multiply clamps exactly its negative part to 0.  Power-of-two
-// scalings round nothing, so sat(x * s_sat) * 2^(25+e) is the rounded
-// relu(scale * x) itself, with no max instruction per element.  Scales beyond
-// 2^100 (or NaN) fall back to the plain multiply-and-max form.
-struct KeyScale {
-  float s_sat;    // multiplier applied to every product
-  float unscale;  // multiplier applied to the head sum
-  bool by_sat;    // the saturating form is exact for this key
-};
+// Fast path (scale >= 0 and finite): relu(scale * x) = scale * relu(x), so
+// every element needs only relu(x) and the key's scale multiplies the head
+// sum once.  The ReLU is split across two pipes: for half of the columns an
+// integer max with 0 on the float's bits (negative floats, -0 included, are
+// negative integers; ALU pipe), for the other half a saturating multiply by
+// 2^-25 (FMA pipe).  For E4M3 operands |q.k| <= 128 * 448^2 < 2^25, so
+// x * 2^-25 lies in (-1, 1): the saturation clamps exactly the negative part
+// to 0 and, being a power of two, rounds nothing; that half's head sum is
+// scaled back by 2^25.  Keys with a negative or non-finite scale take the
+// plain multiply-and-max form.
+constexpr float kSatDown = 0x1p-25f;
+constexpr float kSatUp = 0x1p25f;
 
-__device__ __forceinline__ KeyScale key_scale(float scale) {
-  KeyScale k;
-  int e = 0;
-  frexpf(scale, &e);
-  e = max(e, -100);
-  k.by_sat = fabsf(scale) <= 0x1p100f;
-  k.s_sat = k.by_sat ? ldexpf(scale, -(25 + e)) : scale;
-  k.unscale = k.by_sat ? ldexpf(1.f, 25 + e) : 1.f;
-  return k;
-}
-
-// The fast path splits the ReLU between two pipes.  Key g (scale >= 0):
-// relu(scale * x) = scale * relu(x), and relu of a float is a signed-integer
-// max with 0 on its bits (negative floats, -0 included, are negative
-// integers) on the ALU pipe; its head sum is scaled once.  Key g + 8: the
-// exact saturating multiply on the FMA pipe (see KeyScale).  Both feed a
-// packed f32x2 FMA over the column pairs the load already delivers adjacent.
-template <int H>
-__device__ __forceinline__ void accumulate_half_pos(const float (&v)[64], const float* w_slab, int c,
-                                                    float s_sat1, uint64_t (&a)[kCols / H][2]) {
+// One 64-column read of a unit: x holds this thread's key at slab columns
+// C0 .. C0 + 63.  Weights are the same for every key, so each 16-byte
+// shared-memory load is a broadcast serving 4 columns.  ai / as accumulate
+// per slab row (column pairs packed, f32x2): the integer-max columns and the
+// saturating columns on the fast path, simply the even and odd column pairs
+// of each group of 4 otherwise.
+template <int H, int C0, bool kFast>
+__device__ __forceinline__ void accumulate64(const float (&x)[64], const float* w_slab, float scale,
+                                             uint64_t (&ai)[kCols / H], uint64_t (&as)[kCols / H]) {
 #pragma unroll
-  for (int r = 0; r < 16; ++r) {
-    const int row = (8 * r) / H;
-    const float2 w2 = *reinterpret_cast<const float2*>(&w_slab[8 * r + 2 * c]);
-    const uint64_t wp = f2_pack(w2.x, w2.y);
-    const float y0 = __int_as_float(max(__float_as_int(v[4 * r]), 0));
-    const float y1 = __int_as_float(max(__float_as_int(v[4 * r + 1]), 0));
-    const float y2 = mul_sat(v[4 * r + 2], s_sat1);
-    const float y3 = mul_sat(v[4 * r + 3], s_sat1);
-    a[row][0] = f2_fma(f2_pack(y0, y1), wp, a[row][0]);
-    a[row][1] = f2_fma(f2_pack(y2, y3), wp, a[row][1]);
+  for (int k = 0; k < 16; ++k) {
+    const int row = (C0 + 4 * k) / H;  // a group of 4 columns never straddles rows (H % 4 == 0)
+    const float4 w4 = *reinterpret_cast<const float4*>(w_slab + C0 + 4 * k);
+    float y0, y1, y2, y3;
+    if (kFast) {
+      y0 = __int_as_float(max(__float_as_int(x[4 * k]), 0));
+      y1 = __int_as_float(max(__float_as_int(x[4 * k + 1]), 0));
+      y2 = mul_sat(x[4 * k + 2], kSatDown);
+      y3 = mul_sat(x[4 * k + 3], kSatDown);
+    } else {
+      y0 = fmaxf(x[4 * k] * scale, 0.f);
+      y1 = fmaxf(x[4 * k + 1] * scale, 0.f);
+      y2 = fmaxf(x[4 * k + 2] * scale, 0.f);
+      y3 = fmaxf(x[4 * k + 3] * scale, 0.f);
+    }
+    ai[row] = f2_fma(f2_pack(y0, y1), f2_pack(w4.x, w4.y), ai[row]);
+    as[row] = f2_fma(f2_pack(y2, y3), f2_pack(w4.z, w4.w), as[row]);
   }
 }
 
-// One 16-lane half of a warp's 32 keys: v holds keys g (v[4r], v[4r+1]) and
-// g + 8 (v[4r+2], v[4r+3]) at slab columns 8r + 2c and 8r + 2c + 1.
-// Accumulates w * relu(scale * x) per (row of the slab, key, column parity)
-// in scalar registers: one saturating multiply and one FMA per element.
-template <int H, bool kSat>
-__device__ __forceinline__ void accumulate_half(const float (&v)[64], const float* w_slab, int c,
-                                                const KeyScale& k0, const KeyScale& k1,
-                                                float (&a)[kCols / H][2][2]) {
+// The head sums of one unit for this thread's key: z[r] for the slab's rows.
+template <int H, bool kFast>
+__device__ __forceinline__ void unit_sums(uint32_t taddr, const float* w_slab, float scale,
+                                          uint64_t* t_empty, int lane, float (&z)[kCols / H]) {
+  constexpr int R = kCols / H;
+  uint64_t ai[R], as[R];
 #pragma unroll
-  for (int r = 0; r < 16; ++r) {
-    const int row = (8 * r) / H;  // a repetition's 8 columns never straddle rows (H % 8 == 0)
-    const float2 w2 = *reinterpret_cast<const float2*>(&w_slab[8 * r + 2 * c]);
-    float y0, y1, y2, y3;
-    if (kSat) {
-      y0 = mul_sat(v[4 * r], k0.s_sat);
-      y1 = mul_sat(v[4 * r + 1], k0.s_sat);
-      y2 = mul_sat(v[4 * r + 2], k1.s_sat);
-      y3 = mul_sat(v[4 * r + 3], k1.s_sat);
-    } else {
-      y0 = fmaxf(v[4 * r] * k0.s_sat, 0.f);
-      y1 = fmaxf(v[4 * r + 1] * k0.s_sat, 0.f);
-      y2 = fmaxf(v[4 * r + 2] * k1.s_sat, 0.f);
-      y3 = fmaxf(v[4 * r + 3] * k1.s_sat, 0.f);
-    }
-    a[row][0][0] = fmaf(y0, w2.x, a[row][0][0]);
-    a[row][0][1] = fmaf(y1, w2.y, a[row][0][1]);
-    a[row][1][0] = fmaf(y2, w2.x, a[row][1][0]);
-    a[row][1][1] = fmaf(y3, w2.y, a[row][1][1]);
+  for (int r = 0; r < R; ++r) ai[r] = as[r] = f2_pack(0.f, 0.f);
+  float x[64];
+  tmem_ld64_wait(taddr, x);
+  accumulate64<H, 0, kFast>(x, w_slab, scale, ai, as);
+  tmem_ld64_wait(taddr + 64, x);
+  // The whole buffer is in registers: hand it back.
+  tc_fence_before_sync();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(t_empty);
+  accumulate64<H, 64, kFast>(x, w_slab, scale, ai, as);
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    float i0, i1, s0, s1;
+    f2_unpack(ai[r], i0, i1);
+    f2_unpack(as[r], s0, s1);
+    z[r] = kFast ? scale * fmaf(s0 + s1, kSatUp, i0 + i1) : (i0 + i1) + (s0 + s1);
   }
 }
 
@@ -329,159 +322,67 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int wg = warp / 4;       // this warpgroup's units: wg, wg + 3, ...
     const int quad = warp % 4;     // tensor-memory lanes 32 quad .. 32 quad + 31
-    const int g = lane / 4, c = lane % 4;
-    // Before the head sum, a thread's keys are (half hf, kp): quad*32 + 16 hf
-    // + g + 8 kp; after it, the thread owns one key per row.
-    const int j_off = quad * 32 + 16 * (c >> 1) + g + 8 * (c & 1);
+    const int jl = quad * 32 + lane;  // this thread's key within a tile
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     bool ok = true;
     if (n_t > 0)
       ok = __all_sync(0xffffffffu, mbar_wait(&ctl->q_full, 0, p.wait_limit_ns, p.err, 173));
-    // The next tile's per-key scales are loaded a tile ahead and only turned
-    // into KeyScale when that tile starts, so the load's latency stays hidden.
-    float nraw[2][2];
-    auto fetch_scales = [&](int tl) {
-      const int key0 = (t_begin + tl) * kKeys;
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-        for (int kp = 0; kp < 2; ++kp) {
-          const int jj = key0 + quad * 32 + 16 * hf + g + 8 * kp;
-          nraw[hf][kp] = jj < p.S_kv ? p.kv_scale[jj] : 0.f;
-        }
+    // The next tile's scale of this thread's key is loaded a tile ahead, so
+    // the load's latency stays hidden.
+    float next_scale = 0.f;
+    auto fetch_scale = [&](int tl) {
+      const int j = (t_begin + tl) * kKeys + jl;
+      next_scale = j < p.S_kv ? p.kv_scale[j] : 0.f;
     };
-    if (n_t > 0) fetch_scales(0);
+    if (n_t > 0) fetch_scale(0);
     // This warpgroup's units in order: v = wg, wg + 3, ... (tile v / kSlabs,
-    // slab v % kSlabs, buffer v % kBufs).  A unit is read as two 64-register
+    // slab v % kSlabs, buffer v % kBufs).  A unit is read as two 64-column
     // halves; the latency of each load is covered by the other epilogue warps
     // of the SM sub-partition.
     const int n_units = n_t * kSlabs;
-    KeyScale ks[2][2];
-    float kraw[2][2];
-    bool sat = true, pos = true, fast = true;
+    float scale = 0.f;
+    bool fast = true;
     int cur_tl = -1;
     for (int v = wg; v < n_units && ok; v += kEpiGroups) {
       const int tl = v / kSlabs, s = v % kSlabs, b = v % kBufs;
       const int key0 = (t_begin + tl) * kKeys;
       if (tl != cur_tl) {  // this warpgroup visits every tile, in order
         cur_tl = tl;
-        pos = true;
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-          for (int kp = 0; kp < 2; ++kp) {
-            kraw[hf][kp] = nraw[hf][kp];
-            ks[hf][kp] = key_scale(nraw[hf][kp]);
-            pos = pos && nraw[hf][kp] >= 0.f && nraw[hf][kp] <= 3.0e38f;
-          }
-        if (tl + 1 < n_t) fetch_scales(tl + 1);
-        sat = ks[0][0].by_sat && ks[0][1].by_sat && ks[1][0].by_sat && ks[1][1].by_sat;
-        // The path is chosen per warp, never per thread: the branches hold
+        scale = next_scale;
+        if (tl + 1 < n_t) fetch_scale(tl + 1);
+        // The path is chosen per warp, never per thread: it holds
         // warp-collective tensor-memory loads (.sync.aligned), __syncwarp and
         // the barrier arrive, which the whole warp must reach together.
-        pos = __all_sync(0xffffffffu, pos);
-        sat = __all_sync(0xffffffffu, sat);
-        fast = pos && sat;
+        fast = __all_sync(0xffffffffu, scale >= 0.f && scale <= 3.0e38f);
       }
       ok = __all_sync(0xffffffffu,
                       mbar_wait(&ctl->s_full[b], (v / kBufs) & 1, p.wait_limit_ns, p.err, 170));
       if (!ok) break;
       tc_fence_after_sync();
-      const bool live = slab_live(stats->slo[s], stats->shi[s], key0);
-      float u[2][R][2];  // [half][row][key of the pair]: this thread's partial head sums
+      float z[R];
       const float* w_slab = stats->w + s * kCols;
       const uint32_t taddr = lane_addr + kCols * b;
-      if (live && fast) {
-        uint64_t a2[2][R][2];
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-          for (int r = 0; r < R; ++r) a2[hf][r][0] = a2[hf][r][1] = f2_pack(0.f, 0.f);
-        float x[64];
-        tmem_ld16x256b_x16_wait(taddr, x);
-        accumulate_half_pos<H>(x, w_slab, c, ks[0][1].s_sat, a2[0]);
-        tmem_ld16x256b_x16_wait(taddr + (16u << 16), x);
-        // The whole buffer is in registers: hand it back.
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->t_empty[b]);
-        accumulate_half_pos<H>(x, w_slab, c, ks[1][1].s_sat, a2[1]);
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-          for (int r = 0; r < R; ++r)
-#pragma unroll
-            for (int kp = 0; kp < 2; ++kp) {
-              float lo, hi;
-              f2_unpack(a2[hf][r][kp], lo, hi);
-              u[hf][r][kp] = lo + hi;
-            }
-      } else if (live) {
-        float a[2][R][2][2];  // [half][row][key of the pair][column parity]
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-          for (int r = 0; r < R; ++r)
-            a[hf][r][0][0] = a[hf][r][0][1] = a[hf][r][1][0] = a[hf][r][1][1] = 0.f;
-        float x[64];
-        tmem_ld16x256b_x16_wait(taddr, x);
-        if (sat)
-          accumulate_half<H, true>(x, w_slab, c, ks[0][0], ks[0][1], a[0]);
+      if (slab_live(stats->slo[s], stats->shi[s], key0)) {
+        if (fast)
+          unit_sums<H, true>(taddr, w_slab, scale, &ctl->t_empty[b], lane, z);
         else
-          accumulate_half<H, false>(x, w_slab, c, ks[0][0], ks[0][1], a[0]);
-        tmem_ld16x256b_x16_wait(taddr + (16u << 16), x);
-        // The whole buffer is in registers: hand it back.
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->t_empty[b]);
-        if (sat)
-          accumulate_half<H, true>(x, w_slab, c, ks[1][0], ks[1][1], a[1]);
-        else
-          accumulate_half<H, false>(x, w_slab, c, ks[1][0], ks[1][1], a[1]);
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-          for (int r = 0; r < R; ++r)
-#pragma unroll
-            for (int kp = 0; kp < 2; ++kp) u[hf][r][kp] = a[hf][r][kp][0] + a[hf][r][kp][1];
+          unit_sums<H, false>(taddr, w_slab, scale, &ctl->t_empty[b], lane, z);
       } else {
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl->t_empty[b]);
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-          for (int r = 0; r < R; ++r) u[hf][r][0] = u[hf][r][1] = 0.f;
+        for (int r = 0; r < R; ++r) z[r] = 0.f;
       }
-      // Head sum across the 4 threads sharing a key: first over the key pair
-      // (lane bit 0 keeps kp = c & 1), then over the halves (bit 1 keeps
-      // hf = c >> 1); each step sends the half this thread does not keep.
-      float z[R];
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        float y[2];
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          const float u0 = u[hf][r][0], u1 = u[hf][r][1];
-          const float keep = (c & 1) ? u1 : u0, send = (c & 1) ? u0 : u1;
-          y[hf] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
-        }
-        const float keep = (c & 2) ? y[1] : y[0], send = (c & 2) ? y[0] : y[1];
-        z[r] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-      }
-      const float unscale =
-          fast ? ((c & 2) ? ((c & 1) ? ks[1][1].unscale : kraw[1][0])
-                          : ((c & 1) ? ks[0][1].unscale : kraw[0][0]))
-              : ((c & 2) ? ((c & 1) ? ks[1][1].unscale : ks[1][0].unscale)
-                         : ((c & 1) ? ks[0][1].unscale : ks[0][0].unscale));
-      const int j = key0 + j_off;
+      // Each row's 32 keys of this warp are 128 contiguous bytes.
+      const int j = key0 + jl;
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         const int lr = s * R + r;
         const int i = row0 + lr;
         const bool inside = j >= stats->lo[lr] && j < stats->hi[lr];
         if (i < p.S_q && j < p.S_kv && (inside || p.clean))
-          p.logits[static_cast<size_t>(i) * p.stride + j] = inside ? z[r] * unscale : -INFINITY;
+          p.logits[static_cast<size_t>(i) * p.stride + j] = inside ? z[r] : -INFINITY;
       }
     }
     if (ok && n_t > 0)
