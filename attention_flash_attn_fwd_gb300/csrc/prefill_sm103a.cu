@@ -406,8 +406,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued = 0;    // K/V loads issued, all units
       int q_loads = 0;   // units whose Q was loaded
       bool ok = true;
+      // The producer runs ahead of the MMAs and waits for free stages most of
+      // the time.  In the 16-bit forms it sleeps between tests, leaving the
+      // issue slots of its scheduler to the softmax warps there (C3 ~1%
+      // faster); with FP8's shorter steps the wake-up delay costs more.
+      auto wait_free = [&](uint64_t* bar, uint32_t parity, int site) {
+        return kFp8 ? mbar_wait(bar, parity, p.wait_limit_ns, p.err, site)
+                    : mbar_wait_sleep(bar, parity, p.wait_limit_ns, p.err, site, 32);
+      };
       auto load_q = [&](const Unit& U, int n, int t) {
-        if (n > 0 && !(ok = mbar_wait(&ctl->q_empty[t], (n - 1) & 1, p.wait_limit_ns, p.err, 16)))
+        if (n > 0 && !(ok = wait_free(&ctl->q_empty[t], (n - 1) & 1, 16)))
           return;
         mbar_arrive_expect_tx(&ctl->q_full[t], C::kTileBytes);
         for (int x = 0; x < C::kBoxes; ++x)
@@ -419,8 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kind = 0; kind < 2; ++kind) {
           const int st = issued % C::kStages;
           const int round = issued / C::kStages;
-          if (round > 0 &&
-              !(ok = mbar_wait(&ctl->kv_empty[st], (round - 1) & 1, p.wait_limit_ns, p.err, 10)))
+          if (round > 0 && !(ok = wait_free(&ctl->kv_empty[st], (round - 1) & 1, 10)))
             return;
           uint8_t* dst = s_kv + st * C::kTileBytes;
           mbar_arrive_expect_tx(&ctl->kv_full[st], C::kTileBytes);
@@ -452,9 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int u = dyn ? atomicAdd(p.sched, 1) : (n == 0 ? static_cast<int>(blockIdx.x) : n_units);
         u = (u >= n_units || *abort_flag) ? -1 : head_major(u);
         const int slot = n & 1;
-        if (n >= 2 &&
-            !(ok = mbar_wait(&ctl->unit_empty[slot], ((n >> 1) - 1) & 1, p.wait_limit_ns, p.err,
-                             17)))
+        if (n >= 2 && !(ok = wait_free(&ctl->unit_empty[slot], ((n >> 1) - 1) & 1, 17)))
           break;
         ctl->unit_ring[slot] = u;
         mbar_arrive(&ctl->unit_full[slot]);  // release: the id is visible to the waiters

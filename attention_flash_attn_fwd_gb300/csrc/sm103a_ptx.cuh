@@ -85,6 +85,24 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   }
 }
 
+// Same as mbar_wait, for a waiter that runs ahead and is in no hurry (a
+// producer waiting for a free stage): between tests the thread sleeps for
+// `sleep_ns`, leaving its scheduler's issue slots to the warps it shares
+// them with.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
+                                                int* err, int site, uint32_t sleep_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    __nanosleep(sleep_ns);
+    if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      record_error(err, kErrWaitTimeout, site);
+      return false;
+    }
+  }
+}
+
 // --------------------------------------------------------------- proxies
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
