@@ -125,6 +125,16 @@ __device__ __forceinline__ void mma_tmem_a(uint32_t d, uint32_t a, uint32_t b_lo
               (acc || kk > 0) ? 1u : 0u);
 }
 
+// Same, with A's two 64-key halves in columns [a, a + 32) and [a + 64, a + 96)
+// (each element-wise group's packed pairs over its own fp32 columns).
+__device__ __forceinline__ void mma_tmem_a_split(uint32_t d, uint32_t a, uint32_t b_lo,
+                                                 uint32_t hi, uint32_t idesc, bool acc) {
+#pragma unroll
+  for (int kk = 0; kk < kT / 16; ++kk)
+    mma_ts_lh(d, a + kk * 8 + (kk >= 4 ? 32 : 0), b_lo + ((kk * 16 * 128) >> 4), hi, idesc,
+              (acc || kk > 0) ? 1u : 0u);
+}
+
 // Row-major 16-bit O/dO row r of 128 columns into 128-byte-swizzled staging
 // (two 64-column panels), from 64 fp32 values per call (columns [64h, 64h+64)).
 template <bool kBF16>
@@ -143,81 +153,26 @@ __device__ __forceinline__ void stage_row(uint8_t* tile, int r, int h, const uin
   }
 }
 
-// Element-wise pass over one 128 x 128 step, in place in tensor memory.  The
-// calling warp owns column group g (columns [64g, 64g + 64)) of its 32 rows:
-// S (fp32, columns [cs, cs+128)) -> P (16-bit pairs, [cs, cs+64)),
-// dP (fp32, [cd, cd+128)) -> dS = P (dP - delta) (16-bit pairs, [cd, cd+64)).
-// Packed pairs of group 1 land on fp32 columns of group 0, so every
-// element-wise warp loads its columns before any of them stores (barrier
-// `bar_id` over all element-wise threads).  `lse2_of(c)` / `delta_of(c)` give
-// the row statistics of the column pair (c, c + 1) as a float2 (dK/dV
-// kernel: per query column; dQ kernel: constant per row); `visible(c)` masks
-// causal and ragged positions and is only evaluated when `masked`.
-template <bool kBF16, bool kMasked, int kHalf, class Lse, class Delta, class Vis>
-__device__ __forceinline__ void ew_compute(const uint32_t (&x)[64], const uint32_t (&y)[64],
-                                           uint32_t (&pp)[16], uint32_t (&dd)[16], int g,
-                                           float c, Lse lse2_of, Delta delta_of, Vis visible) {
-#pragma unroll
-  for (int q = 16 * kHalf; q < 16 * kHalf + 16; ++q) {
-    float pv[2], dv[2];
-    const int col0 = 64 * g + 2 * q;
-    const float2 l2 = lse2_of(col0), dl = delta_of(col0);  // columns col0, col0 + 1
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int col = col0 + e;
-      float pe = ex2_approx(fmaf(__uint_as_float(x[2 * q + e]), c, -(e ? l2.y : l2.x)));
-      if constexpr (kMasked) pe = visible(col) ? pe : 0.f;
-      pv[e] = pe;
-      dv[e] = pe * (__uint_as_float(y[2 * q + e]) - (e ? dl.y : dl.x));
-    }
-    pp[q - 16 * kHalf] = pack2<kBF16>(pv[0], pv[1]);
-    dd[q - 16 * kHalf] = pack2<kBF16>(dv[0], dv[1]);
-  }
-}
-
-template <bool kBF16, class Lse, class Delta, class Vis>
-__device__ __forceinline__ void elementwise_step(uint32_t lane_addr, int g, uint32_t cs,
-                                                 uint32_t cd, float c, bool masked, int bar_id,
-                                                 Lse lse2_of, Delta delta_of, Vis visible) {
-  uint32_t x[64], y[64];
-  tmem_ld64_wait(lane_addr + cs + 64 * g, x);
-  tmem_ld64_wait(lane_addr + cd + 64 * g, y);
-  named_barrier_sync(bar_id, kEwWarps * 32);
-  {
-    uint32_t pp[16], dd[16];
-    if (masked)
-      ew_compute<kBF16, true, 0>(x, y, pp, dd, g, c, lse2_of, delta_of, visible);
-    else
-      ew_compute<kBF16, false, 0>(x, y, pp, dd, g, c, lse2_of, delta_of, visible);
-    tmem_st16(lane_addr + cs + 32 * g, pp);
-    tmem_st16(lane_addr + cd + 32 * g, dd);
-  }
-  {
-    uint32_t pp[16], dd[16];
-    if (masked)
-      ew_compute<kBF16, true, 1>(x, y, pp, dd, g, c, lse2_of, delta_of, visible);
-    else
-      ew_compute<kBF16, false, 1>(x, y, pp, dd, g, c, lse2_of, delta_of, visible);
-    tmem_st16(lane_addr + cs + 32 * g + 16, pp);
-    tmem_st16(lane_addr + cd + 32 * g + 16, dd);
-  }
-  tmem_st_wait();
-}
-
-// The dK/dV kernel's element-wise pass in two phases: P^T for all of the
-// warp's columns is stored and announced on `p_ready` first, so the MMA warp
-// runs dV += P^T dO while the warps compute dS^T = P^T (dP^T - delta).  Same
-// column ownership, barrier and arithmetic as elementwise_step.
+// The dK/dV kernel's element-wise pass over one 128 x 128 step, in place in
+// tensor memory.  The calling warp owns column group g (columns [64g, 64g +
+// 64)) of its 32 rows: S^T (fp32, columns [cs, cs + 128)) -> P^T (16-bit pairs,
+// [cs + 64g, cs + 64g + 32)), dP^T (fp32, [cd, cd + 128)) -> dS^T = P^T (dP^T -
+// delta) (16-bit pairs, [cd + 64g, cd + 64g + 32)): each group's pairs land on
+// its own fp32 columns, already in its registers, so no warp waits for
+// another before storing (the MMAs read A from the two 32-column ranges).
+// P^T is stored and announced on `p_ready` first, so the MMA warp runs dV +=
+// P^T dO while the warps compute dS^T.  `lse2_of(c)` / `delta_of(c)` give the
+// row statistics of the column pair (c, c + 1) as a float2 (per query
+// column); `visible(c)` masks causal and ragged positions and is only
+// evaluated when kMasked.
 template <bool kBF16, bool kMasked, class Lse, class Delta, class Vis>
 __device__ __forceinline__ void elementwise_step_p_first(uint32_t lane_addr, int g, uint32_t cs,
-                                                         uint32_t cd, float c, int bar_id,
-                                                         Lse lse2_of, Delta delta_of,
-                                                         Vis visible, uint64_t* p_ready,
-                                                         int lane) {
+                                                         uint32_t cd, float c, Lse lse2_of,
+                                                         Delta delta_of, Vis visible,
+                                                         uint64_t* p_ready, int lane) {
   uint32_t x[64], y[64];
   tmem_ld64_wait(lane_addr + cs + 64 * g, x);
   tmem_ld64_wait(lane_addr + cd + 64 * g, y);
-  named_barrier_sync(bar_id, kEwWarps * 32);
   // Column pairs in packed fp32 (f32x2): one instruction per two elements.
   const uint64_t c2 = f2_pack(c, c);
 #pragma unroll
@@ -240,7 +195,7 @@ __device__ __forceinline__ void elementwise_step_p_first(uint32_t lane_addr, int
       x[2 * q + 1] = __float_as_uint(p1);
       pp[q - 16 * hf] = pack2<kBF16>(p0, p1);
     }
-    tmem_st16(lane_addr + cs + 32 * g + 16 * hf, pp);
+    tmem_st16(lane_addr + cs + 64 * g + 16 * hf, pp);
   }
   tmem_st_wait();
   tc_fence_before_sync();
@@ -261,7 +216,7 @@ __device__ __forceinline__ void elementwise_step_p_first(uint32_t lane_addr, int
                 d0, d1);
       dd[q - 16 * hf] = pack2<kBF16>(d0, d1);
     }
-    tmem_st16(lane_addr + cd + 32 * g + 16 * hf, dd);
+    tmem_st16(lane_addr + cd + 64 * g + 16 * hf, dd);
   }
   tmem_st_wait();
 }
@@ -427,10 +382,10 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         // then dK += dS^T Q; the walking tiles are read MN-major.
         if (!(ok = mbar_wait(&ctl->p_ready, s & 1, p.wait_limit_ns, p.err, 68))) break;
         tc_fence_after_sync();
-        mma_tmem_a(tmem + 256, tmem + 0, sdesc_lo(stage + kTile, kPanel), hi, id_o, s > 0);
+        mma_tmem_a_split(tmem + 256, tmem + 0, sdesc_lo(stage + kTile, kPanel), hi, id_o, s > 0);
         if (!(ok = mbar_wait(&ctl->ew_done, s & 1, p.wait_limit_ns, p.err, 65))) break;
         tc_fence_after_sync();
-        mma_tmem_a(tmem + 384, tmem + 128, sdesc_lo(stage, kPanel), hi, id_o, s > 0);
+        mma_tmem_a_split(tmem + 384, tmem + 128, sdesc_lo(stage, kPanel), hi, id_o, s > 0);
         mma_commit(&ctl->empty[st]);
       }
       if (!ok) *abort_flag = 1;
@@ -467,10 +422,10 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         return key < p.S_kv && i < p.S_q && (!p.causal || key <= i + off);
       };
       if (full)
-        elementwise_step_p_first<kBF16, false>(lane_addr, g, 0, 128, p.scale_log2, 2, lse2_of,
+        elementwise_step_p_first<kBF16, false>(lane_addr, g, 0, 128, p.scale_log2, lse2_of,
                                                delta_of, visible, &ctl->p_ready, lane);
       else
-        elementwise_step_p_first<kBF16, true>(lane_addr, g, 0, 128, p.scale_log2, 2, lse2_of,
+        elementwise_step_p_first<kBF16, true>(lane_addr, g, 0, 128, p.scale_log2, lse2_of,
                                               delta_of, visible, &ctl->p_ready, lane);
       tc_fence_before_sync();
       __syncwarp();
