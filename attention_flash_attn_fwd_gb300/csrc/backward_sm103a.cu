@@ -370,23 +370,49 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       const uint32_t k_lo = sdesc_lo(smem_u32(s_k), 16);
       const uint32_t v_lo = sdesc_lo(smem_u32(s_v), 16);
       bool ok = mbar_wait(&ctl->res_full, 0, p.wait_limit_ns, p.err, 63);
-      for (int s = 0; s < n_steps && ok; ++s) {
-        const int st = s % kRing;
-        const uint32_t stage = smem_u32(smem + kOffRing + st * 2 * kTile);
-        if (!(ok = mbar_wait(&ctl->full[st], (s / kRing) & 1, p.wait_limit_ns, p.err, 64))) break;
+      auto stage_of = [&](int s) { return smem_u32(smem + kOffRing + (s % kRing) * 2 * kTile); };
+      auto wait_stage = [&](int s) {
+        const bool w = mbar_wait(&ctl->full[s % kRing], (s / kRing) & 1, p.wait_limit_ns, p.err, 64);
         tc_fence_after_sync();
-        mma_abt(tmem + 0, k_lo, sdesc_lo(stage, 16), hi, id_s);            // S^T = K Q^T
-        mma_abt(tmem + 128, v_lo, sdesc_lo(stage + kTile, 16), hi, id_s);  // dP^T = V dO^T
+        return w;
+      };
+      // Step s: S^T_s = K Q_s^T into [0, 128), dP^T_s = V dO_s^T into [128, 256);
+      // dV += P^T_s dO_s once P^T is in place (while dS^T is computed), then
+      // dK += dS^T_s Q_s (the walking tiles read MN-major).  The element-wise
+      // warps hold S^T_s, dP^T_s and the fp32 P^T_s in registers, so S^T_{s+1}
+      // may run right after dV_s has read P^T_s from S's columns, during the
+      // dS^T pass -- if the next tiles have already landed (waiting for them
+      // there would hold back dK_s); else it follows dK_s.  dP^T_{s+1} always
+      // follows dK_s, which reads dS^T_s from dP's columns.
+      if (ok && (ok = wait_stage(0))) {
+        mma_abt(tmem + 0, k_lo, sdesc_lo(stage_of(0), 16), hi, id_s);
+        mma_abt(tmem + 128, v_lo, sdesc_lo(stage_of(0) + kTile, 16), hi, id_s);
         mma_commit(&ctl->mm_full);
-        // dV += P^T dO as soon as P^T is in place (while dS^T is computed),
-        // then dK += dS^T Q; the walking tiles are read MN-major.
+      }
+      for (int s = 0; s < n_steps && ok; ++s) {
+        const uint32_t stage = stage_of(s);
+        const bool next = s + 1 < n_steps;
         if (!(ok = mbar_wait(&ctl->p_ready, s & 1, p.wait_limit_ns, p.err, 68))) break;
         tc_fence_after_sync();
         mma_tmem_a_split(tmem + 256, tmem + 0, sdesc_lo(stage + kTile, kPanel), hi, id_o, s > 0);
+        bool s_early = false;
+        if (next && mbar_test_wait(&ctl->full[(s + 1) % kRing], ((s + 1) / kRing) & 1)) {
+          tc_fence_after_sync();
+          mma_abt(tmem + 0, k_lo, sdesc_lo(stage_of(s + 1), 16), hi, id_s);
+          s_early = true;
+        }
         if (!(ok = mbar_wait(&ctl->ew_done, s & 1, p.wait_limit_ns, p.err, 65))) break;
         tc_fence_after_sync();
         mma_tmem_a_split(tmem + 384, tmem + 128, sdesc_lo(stage, kPanel), hi, id_o, s > 0);
-        mma_commit(&ctl->empty[st]);
+        mma_commit(&ctl->empty[s % kRing]);
+        if (next) {
+          if (!s_early) {
+            if (!(ok = wait_stage(s + 1))) break;
+            mma_abt(tmem + 0, k_lo, sdesc_lo(stage_of(s + 1), 16), hi, id_s);
+          }
+          mma_abt(tmem + 128, v_lo, sdesc_lo(stage_of(s + 1) + kTile, 16), hi, id_s);
+          mma_commit(&ctl->mm_full);
+        }
       }
       if (!ok) *abort_flag = 1;
       mma_commit(&ctl->mma_done);
