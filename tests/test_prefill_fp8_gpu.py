@@ -43,6 +43,20 @@ def test_prefill_fp8_matches_oracle(B, H, S_q, S_kv, causal, layout):
     assert_lse_close(lse, ref_lse, "fp8 lse %s" % (case,))
 
 
+def test_prefill_fp8_persistent_runs_of_units_without_keys():
+    """The FP8 form over more units than SMs with most tiles seeing no key
+    (causal, S_kv far below S_q): runs of keyless units back to back in the
+    persistent CTAs, one unit whose first tile only has no key."""
+    case = workloads.Fp8PrefillCase("t", 2, 80, 2048, 374, 128, "bshd", True, seed=43)
+    inputs, o, lse = _run(case)
+    ref_o, ref_lse = _ref(inputs, case)
+    assert_close(o, ref_o, "fp8 %s" % (case,), FP8_MAX_ABS, FP8_REL_L2)
+    assert_lse_close(lse, ref_lse, "fp8 lse %s" % (case,))
+    dead = 2048 - 374
+    assert torch.all(o[:, :dead] == 0)
+    assert torch.all(torch.isneginf(lse[:, :, :dead]))
+
+
 def test_prefill_fp8_fp16_output():
     case = workloads.Fp8PrefillCase("t", 2, 2, 300, 300, 128, "bhsd", True, seed=42)
     inputs, o, lse = _run(case, out_dtype=torch.float16)

@@ -59,6 +59,23 @@ def test_prefill_sweep_matches_oracle(shape, causal, layout, dtype, D):
     _check_full(case)
 
 
+@pytest.mark.parametrize("D,dtype,layout", [(128, "bf16", "bshd"), (64, "fp16", "bhsd")])
+def test_persistent_runs_of_units_without_keys(D, dtype, layout):
+    """Causal with far fewer keys than queries (bottom-right alignment) over
+    more units than SMs: rows before S_q - S_kv see no key, so six of a head's
+    eight units have no key in either tile, one has none in its first tile
+    only (the diagonal offset 1674 falls inside its second tile), and the
+    persistent CTAs take such units back to back.  Those rows are exact zeros
+    with lse = -inf; the rest matches the oracle."""
+    S_q, S_kv = 2048, 374
+    case = workloads.PrefillCase("nokeys", 2, 80, S_q, S_kv, D, layout, dtype, True, seed=13)
+    o, lse = _check_full(case)
+    dead = S_q - S_kv
+    o_dead = o[:, :dead] if layout == "bshd" else o[:, :, :dead]
+    assert torch.all(o_dead == 0)
+    assert torch.all(torch.isneginf(lse[:, :, :dead]))
+
+
 def test_empty_kv_gives_zero_and_neg_inf_lse():
     q = torch.randn(1, 2, 40, 64, dtype=torch.float16, device="cuda")
     k = torch.empty(1, 2, 0, 64, dtype=torch.float16, device="cuda")
