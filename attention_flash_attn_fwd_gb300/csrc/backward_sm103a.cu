@@ -223,29 +223,46 @@ __device__ __forceinline__ void elementwise_step_p_first(uint32_t lane_addr, int
 
 // ---------------------------------------------------------------- delta
 
-// delta[b,h,i] = sum_d dO[b,h,i,d] * O[b,h,i,d] in fp32; one warp per row.
+// delta[b,h,i] = sum_d dO[b,h,i,d] * O[b,h,i,d] in fp32.  HBM-bound: 16
+// lanes read a row as 16-byte pieces (o and dout are 16-byte aligned,
+// checked on the host), a warp takes kDeltaRows rows and issues all of its
+// loads before the first reduction, so enough bytes are in flight to stream
+// at the copy rate.
+constexpr int kDeltaRows = 8;  // rows per warp: 2 per pass (one per half-warp), 4 passes
 template <bool kBF16>
 __global__ void __launch_bounds__(256) bwd_delta_kernel(const BackwardParams p) {
   using T = typename std::conditional<kBF16, __nv_bfloat16, __half>::type;
+  constexpr int kPasses = kDeltaRows / 2;
   const long long rows = static_cast<long long>(p.B) * p.H * p.S_q;
-  const long long row = static_cast<long long>(blockIdx.x) * 8 + threadIdx.x / 32;
-  const int lane = threadIdx.x % 32;
-  if (row >= rows) return;
-  const int i = static_cast<int>(row % p.S_q);
-  const int bh = static_cast<int>(row / p.S_q);
-  const int b = bh / p.H, h = bh % p.H;
-  const size_t off = p.bshd ? ((static_cast<size_t>(b) * p.S_q + i) * p.H + h) * kT
-                            : ((static_cast<size_t>(b) * p.H + h) * p.S_q + i) * kT;
-  const uint2 a = *reinterpret_cast<const uint2*>(static_cast<const T*>(p.o) + off + lane * 4);
-  const uint2 g = *reinterpret_cast<const uint2*>(static_cast<const T*>(p.dout) + off + lane * 4);
-  const T* av = reinterpret_cast<const T*>(&a);
-  const T* gv = reinterpret_cast<const T*>(&g);
-  float s = 0.f;
+  const int lane = threadIdx.x % 32, half = lane / 16, l16 = lane % 16;
+  const long long row0 = (static_cast<long long>(blockIdx.x) * 8 + threadIdx.x / 32) * kDeltaRows;
+  uint4 a[kPasses], g[kPasses];
 #pragma unroll
-  for (int e = 0; e < 4; ++e) s += static_cast<float>(av[e]) * static_cast<float>(gv[e]);
+  for (int k = 0; k < kPasses; ++k) {
+    const long long row = row0 + 2 * k + half;
+    a[k] = g[k] = make_uint4(0u, 0u, 0u, 0u);
+    if (row < rows) {
+      const int i = static_cast<int>(row % p.S_q);
+      const int bh = static_cast<int>(row / p.S_q);
+      const int b = bh / p.H, h = bh % p.H;
+      const size_t off = (p.bshd ? ((static_cast<size_t>(b) * p.S_q + i) * p.H + h) * kT
+                                 : static_cast<size_t>(row) * kT) + l16 * 8;
+      a[k] = __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(p.o) + off));
+      g[k] = __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(p.dout) + off));
+    }
+  }
 #pragma unroll
-  for (int m = 16; m > 0; m >>= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
-  if (lane == 0) p.delta[row] = s;
+  for (int k = 0; k < kPasses; ++k) {
+    const T* av = reinterpret_cast<const T*>(&a[k]);
+    const T* gv = reinterpret_cast<const T*>(&g[k]);
+    float s = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) s = fmaf(static_cast<float>(av[e]), static_cast<float>(gv[e]), s);
+#pragma unroll
+    for (int m = 8; m > 0; m >>= 1) s += __shfl_xor_sync(0xffffffffu, s, m);  // within the half
+    const long long row = row0 + 2 * k + half;
+    if (l16 == 0 && row < rows) p.delta[row] = s;
+  }
 }
 
 // ---------------------------------------------------------------- dK / dV
@@ -768,7 +785,8 @@ cudaError_t launch_all(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
   if (ce != cudaSuccess) return ce;
   const long long rows = static_cast<long long>(p.B) * p.H * p.S_q;
   if (rows > 0) {
-    bwd_delta_kernel<kBF16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(p);
+    bwd_delta_kernel<kBF16><<<static_cast<unsigned>((rows + 8 * kDeltaRows - 1) / (8 * kDeltaRows)),
+                              256, 0, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
