@@ -65,7 +65,8 @@ struct BwdCtl {
   uint64_t res_full;          // the resident pair of tiles has landed
   uint64_t full[kRing];       // walking pair (+ its lse/delta rows) has landed
   uint64_t empty[kRing];      // the MMAs reading a stage are done
-  uint64_t mm_full;           // the two products of a step are in tensor memory
+  uint64_t s_full;            // dK/dV kernel: S^T of a step is in tensor memory
+  uint64_t dp_full;           // dK/dV kernel: dP^T of a step is in tensor memory
   uint64_t p_ready;           // dK/dV kernel: P^T of a step is in tensor memory
   uint64_t ew_done;           // the element-wise pass of a step is in tensor memory
   uint64_t mma_done;          // every MMA of the CTA has completed
@@ -160,19 +161,22 @@ __device__ __forceinline__ void stage_row(uint8_t* tile, int r, int h, const uin
 // delta) (16-bit pairs, [cd + 64g, cd + 64g + 32)): each group's pairs land on
 // its own fp32 columns, already in its registers, so no warp waits for
 // another before storing (the MMAs read A from the two 32-column ranges).
-// P^T is stored and announced on `p_ready` first, so the MMA warp runs dV +=
-// P^T dO while the warps compute dS^T.  `lse2_of(c)` / `delta_of(c)` give the
-// row statistics of the column pair (c, c + 1) as a float2 (per query
-// column); `visible(c)` masks causal and ragged positions and is only
-// evaluated when kMasked.
+// S^T and dP^T arrive separately (`s_full`, `dp_full`): P^T is computed from
+// S^T alone, stored and announced on `p_ready`, and only then is dP^T waited
+// for and read, so the MMA warp can run dK of the previous step and dP^T of
+// this one while P^T is computed.  `lse2_of(c)` / `delta_of(c)` give the row
+// statistics of the column pair (c, c + 1) as a float2 (per query column);
+// `visible(c)` masks causal and ragged positions and is only evaluated when
+// kMasked.  Returns false if the wait for dP^T timed out.
 template <bool kBF16, bool kMasked, class Lse, class Delta, class Vis>
-__device__ __forceinline__ void elementwise_step_p_first(uint32_t lane_addr, int g, uint32_t cs,
+__device__ __forceinline__ bool elementwise_step_p_first(uint32_t lane_addr, int g, uint32_t cs,
                                                          uint32_t cd, float c, Lse lse2_of,
                                                          Delta delta_of, Vis visible,
-                                                         uint64_t* p_ready, int lane) {
+                                                         uint64_t* p_ready, uint64_t* dp_full,
+                                                         uint32_t dp_parity, uint64_t limit_ns,
+                                                         int* err, int lane) {
   uint32_t x[64], y[64];
   tmem_ld64_wait(lane_addr + cs + 64 * g, x);
-  tmem_ld64_wait(lane_addr + cd + 64 * g, y);
   // Column pairs in packed fp32 (f32x2): one instruction per two elements.
   const uint64_t c2 = f2_pack(c, c);
 #pragma unroll
@@ -201,6 +205,9 @@ __device__ __forceinline__ void elementwise_step_p_first(uint32_t lane_addr, int
   tc_fence_before_sync();
   __syncwarp();
   if (lane == 0) mbar_arrive(p_ready);
+  if (!__all_sync(0xffffffffu, mbar_wait(dp_full, dp_parity, limit_ns, err, 72))) return false;
+  tc_fence_after_sync();
+  tmem_ld64_wait(lane_addr + cd + 64 * g, y);
 #pragma unroll
   for (int hf = 0; hf < 2; ++hf) {
     uint32_t dd[16];
@@ -219,6 +226,7 @@ __device__ __forceinline__ void elementwise_step_p_first(uint32_t lane_addr, int
     tmem_st16(lane_addr + cd + 64 * g + 16 * hf, dd);
   }
   tmem_st_wait();
+  return true;
 }
 
 // ---------------------------------------------------------------- delta
@@ -306,7 +314,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       mbar_init(&ctl->full[s], 2);  // TMA bytes + the row statistics
       mbar_init(&ctl->empty[s], 1);
     }
-    mbar_init(&ctl->mm_full, 1);
+    mbar_init(&ctl->s_full, 1);
+    mbar_init(&ctl->dp_full, 1);
     mbar_init(&ctl->p_ready, kEwWarps);
     mbar_init(&ctl->ew_done, kEwWarps);
     mbar_init(&ctl->mma_done, 1);
@@ -334,25 +343,12 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       for (int s = 0; s < n_steps; ++s) {
         if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
         const int st = s % kRing;
-        bool ok = true;
-        if (lane == 0 && s >= kRing)
-          ok = mbar_wait(&ctl->empty[st], (s / kRing - 1) & 1, p.wait_limit_ns, p.err, 60);
-        if (!__shfl_sync(0xffffffffu, ok, 0)) {
-          if (lane == 0) *abort_flag = 1;
-          break;
-        }
         const int q0 = (first + s) * kT;
-        uint8_t* stage = smem + kOffRing + st * 2 * kTile;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&ctl->full[st], 2 * kTile);
-          load_tile(stage, &tm_q, &ctl->full[st], q0, h, b, p.bshd);
-          load_tile(stage + kTile, &tm_do, &ctl->full[st], q0, h, b, p.bshd);
-        }
-        // The tile's row statistics: all eight global loads of a lane are
-        // issued before any shared-memory store (a store between them, which
-        // the compiler cannot prove distinct from the next load, serialised
-        // eight memory round trips: ~7000 cycles per step, measured on GB300).
-        float* rows = s_rows + st * 2 * kT;
+        // The tile's row statistics: every global load of a lane is issued
+        // before any shared-memory store (a store between them, which the
+        // compiler cannot prove distinct from the next load, serialised eight
+        // memory round trips: ~7000 cycles per step, measured on GB300), and
+        // before the wait for a free stage, so their latency overlaps it.
         const float* lse_b = p.lse + static_cast<size_t>(bh) * p.S_q;
         const float* dlt_b = p.delta + static_cast<size_t>(bh) * p.S_q;
         float lv[kT / 32], dv[kT / 32];
@@ -362,6 +358,20 @@ __global__ void __launch_bounds__(kThreadsB, 1)
           lv[k] = i < p.S_q ? __ldg(lse_b + i) : 0.f;
           dv[k] = i < p.S_q ? __ldg(dlt_b + i) : 0.f;
         }
+        bool ok = true;
+        if (lane == 0 && s >= kRing)
+          ok = mbar_wait(&ctl->empty[st], (s / kRing - 1) & 1, p.wait_limit_ns, p.err, 60);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
+          if (lane == 0) *abort_flag = 1;
+          break;
+        }
+        uint8_t* stage = smem + kOffRing + st * 2 * kTile;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&ctl->full[st], 2 * kTile);
+          load_tile(stage, &tm_q, &ctl->full[st], q0, h, b, p.bshd);
+          load_tile(stage + kTile, &tm_do, &ctl->full[st], q0, h, b, p.bshd);
+        }
+        float* rows = s_rows + st * 2 * kT;
 #pragma unroll
         for (int k = 0; k < kT / 32; ++k) {
           rows[lane + 32 * k] = lv[k] * kLog2e;
@@ -393,18 +403,18 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         tc_fence_after_sync();
         return w;
       };
-      // Step s: S^T_s = K Q_s^T into [0, 128), dP^T_s = V dO_s^T into [128, 256);
-      // dV += P^T_s dO_s once P^T is in place (while dS^T is computed), then
-      // dK += dS^T_s Q_s (the walking tiles read MN-major).  The element-wise
-      // warps hold S^T_s, dP^T_s and the fp32 P^T_s in registers, so S^T_{s+1}
-      // may run right after dV_s has read P^T_s from S's columns, during the
-      // dS^T pass -- if the next tiles have already landed (waiting for them
-      // there would hold back dK_s); else it follows dK_s.  dP^T_{s+1} always
-      // follows dK_s, which reads dS^T_s from dP's columns.
+      // Step s: S^T_s = K Q_s^T into [0, 128) (signalled on s_full), dP^T_s = V
+      // dO_s^T into [128, 256) (dp_full); dV += P^T_s dO_s once P^T is in place,
+      // dK += dS^T_s Q_s once dS^T is (the walking tiles read MN-major).  S^T_{s+1}
+      // follows dV_s, which has read P^T_s from S's columns, and dP^T_{s+1}
+      // follows dK_s, which has read dS^T_s from dP's columns: the element-wise
+      // warps start P^T_{s+1} from S^T_{s+1} alone while the tensor core runs
+      // dK_s and dP^T_{s+1}.
       if (ok && (ok = wait_stage(0))) {
         mma_abt(tmem + 0, k_lo, sdesc_lo(stage_of(0), 16), hi, id_s);
+        mma_commit(&ctl->s_full);
         mma_abt(tmem + 128, v_lo, sdesc_lo(stage_of(0) + kTile, 16), hi, id_s);
-        mma_commit(&ctl->mm_full);
+        mma_commit(&ctl->dp_full);
       }
       for (int s = 0; s < n_steps && ok; ++s) {
         const uint32_t stage = stage_of(s);
@@ -412,23 +422,27 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         if (!(ok = mbar_wait(&ctl->p_ready, s & 1, p.wait_limit_ns, p.err, 68))) break;
         tc_fence_after_sync();
         mma_tmem_a_split(tmem + 256, tmem + 0, sdesc_lo(stage + kTile, kPanel), hi, id_o, s > 0);
-        bool s_early = false;
+        // S^T_{s+1} goes first if its tiles have landed (a non-blocking test):
+        // waiting for them here would hold back dK_s.
+        bool s_next = false;
         if (next && mbar_test_wait(&ctl->full[(s + 1) % kRing], ((s + 1) / kRing) & 1)) {
           tc_fence_after_sync();
           mma_abt(tmem + 0, k_lo, sdesc_lo(stage_of(s + 1), 16), hi, id_s);
-          s_early = true;
+          mma_commit(&ctl->s_full);
+          s_next = true;
         }
         if (!(ok = mbar_wait(&ctl->ew_done, s & 1, p.wait_limit_ns, p.err, 65))) break;
         tc_fence_after_sync();
         mma_tmem_a_split(tmem + 384, tmem + 128, sdesc_lo(stage, kPanel), hi, id_o, s > 0);
         mma_commit(&ctl->empty[s % kRing]);
         if (next) {
-          if (!s_early) {
+          if (!s_next) {
             if (!(ok = wait_stage(s + 1))) break;
             mma_abt(tmem + 0, k_lo, sdesc_lo(stage_of(s + 1), 16), hi, id_s);
+            mma_commit(&ctl->s_full);
           }
           mma_abt(tmem + 128, v_lo, sdesc_lo(stage_of(s + 1) + kTile, 16), hi, id_s);
-          mma_commit(&ctl->mm_full);
+          mma_commit(&ctl->dp_full);
         }
       }
       if (!ok) *abort_flag = 1;
@@ -449,7 +463,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
     bool ok = true;
     for (int s = 0; s < n_steps; ++s) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&ctl->mm_full, s & 1, p.wait_limit_ns, p.err, 70));
+      ok = __all_sync(0xffffffffu, mbar_wait(&ctl->s_full, s & 1, p.wait_limit_ns, p.err, 70));
       if (!ok) break;
       tc_fence_after_sync();
       const int st = s % kRing;
@@ -465,11 +479,16 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         return key < p.S_kv && i < p.S_q && (!p.causal || key <= i + off);
       };
       if (full)
-        elementwise_step_p_first<kBF16, false>(lane_addr, g, 0, 128, p.scale_log2, lse2_of,
-                                               delta_of, visible, &ctl->p_ready, lane);
+        ok = elementwise_step_p_first<kBF16, false>(lane_addr, g, 0, 128, p.scale_log2, lse2_of,
+                                                    delta_of, visible, &ctl->p_ready,
+                                                    &ctl->dp_full, s & 1, p.wait_limit_ns, p.err,
+                                                    lane);
       else
-        elementwise_step_p_first<kBF16, true>(lane_addr, g, 0, 128, p.scale_log2, lse2_of,
-                                              delta_of, visible, &ctl->p_ready, lane);
+        ok = elementwise_step_p_first<kBF16, true>(lane_addr, g, 0, 128, p.scale_log2, lse2_of,
+                                                   delta_of, visible, &ctl->p_ready,
+                                                   &ctl->dp_full, s & 1, p.wait_limit_ns, p.err,
+                                                   lane);
+      if (!ok) break;
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->ew_done);
