@@ -49,6 +49,7 @@ constexpr int kThreadsB = 384;  // 8 element-wise warps | TMA warp, MMA warp, 2 
 constexpr int kEwWarps = 8;
 constexpr int kWarpLoad = 8;
 constexpr int kWarpMmaB = 9;
+constexpr int kWarpMmaDq = 10;  // dQ kernel: issues dQ += dS K beside warp 9's S and dP
 // Registers are granted per warpgroup: the block launches with 168 per
 // thread (64512 in all) and setmaxnreg gives the two element-wise warpgroups
 // 200, the control warpgroup 104 (2*128*200 + 128*104 = 64512): with less,
@@ -546,6 +547,7 @@ struct DqCtl {
   uint64_t ds_free;             // dQ_{j-1} has read the dS columns
   uint64_t mma_done;            // every MMA of the CTA has completed
   uint64_t tmem_free;           // the element-wise warps are done with tensor memory
+  uint64_t prod_done;           // warp 9's last products have completed
   uint32_t tmem_base;
   int abort;
 };
@@ -604,6 +606,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     mbar_init(&ctl->ds_free, 1);
     mbar_init(&ctl->mma_done, 1);
     mbar_init(&ctl->tmem_free, kEwWarps);
+    mbar_init(&ctl->prod_done, 1);
     ctl->abort = 0;
     fence_mbar_init();
   }
@@ -671,13 +674,31 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         mma_commit(&ctl->v_empty[sv]);
         return true;
       };
+      // This thread issues the products; dQ += dS_s K_s comes from warp 10's
+      // thread, so the two threads' waits and commits overlap instead of
+      // adding up.  They touch different tensor-memory columns and are
+      // ordered only through the element-wise warps' barriers.
       bool ok = mbar_wait(&ctl->res_full, 0, p.wait_limit_ns, p.err, 83);
       if (ok) ok = products(0);
+      for (int s = 0; s + 1 < n_steps && ok; ++s) {
+        if (!(ok = mbar_wait(&ctl->loaded, s & 1, p.wait_limit_ns, p.err, 88))) break;
+        ok = products(s + 1);
+      }
+      if (!ok) *abort_flag = 1;
+      mma_commit(&ctl->prod_done);
+      mbar_wait(&ctl->prod_done, 0, p.wait_limit_ns, p.err, 86);
+    }
+    __syncwarp();
+    mbar_wait(&ctl->tmem_free, 0, p.wait_limit_ns, p.err, 87);
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 512);
+   } else if (warp == kWarpMmaDq) {
+    // ---------------------------------------------------------- dQ issuer
+    if (lane == 0 && n_steps > 0) {
+      constexpr uint32_t id_o = idesc_f16(kBF16, kT, kT, false, true);
+      const uint32_t hi = sdesc_hi_sw128(1024);
+      bool ok = true;
       for (int s = 0; s < n_steps && ok; ++s) {
-        if (s + 1 < n_steps) {
-          if (!(ok = mbar_wait(&ctl->loaded, s & 1, p.wait_limit_ns, p.err, 88))) break;
-          if (!(ok = products(s + 1))) break;
-        }
         if (!(ok = mbar_wait(&ctl->ew_done, s & 1, p.wait_limit_ns, p.err, 85))) break;
         tc_fence_after_sync();
         // dQ += dS_s K_s (dS in columns [384, 448)), K read MN-major
@@ -685,16 +706,14 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         mma_tmem_a(tmem + 256, tmem + 384, sdesc_lo(smem_u32(s_k + sk * kTile), kPanel), hi, id_o,
                    s > 0);
         mma_commit(&ctl->ds_free);
-        mma_commit(&ctl->k_empty[sk]);
+        mma_commit(&ctl->k_empty[sk]);  // S_s (warp 9) completed before dS_s was published
       }
       if (!ok) *abort_flag = 1;
+      // The last MMAs of the CTA: every product came before the last dS.
       mma_commit(&ctl->mma_done);
-      mbar_wait(&ctl->mma_done, 0, p.wait_limit_ns, p.err, 86);
+      mbar_wait(&ctl->mma_done, 0, p.wait_limit_ns, p.err, 77);
     }
     __syncwarp();
-    mbar_wait(&ctl->tmem_free, 0, p.wait_limit_ns, p.err, 87);
-    tc_fence_after_sync();
-    tmem_dealloc(tmem, 512);
    }
   } else {
     setmaxnreg_inc<kRegsEw>();
