@@ -684,10 +684,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int key0 = j * kBN;
         const bool full = (key0 + kBN <= S_kv) && (!p.causal || key0 + kBN - 1 <= row0 + diag);
         if (!full) {
+          // Keys past L = lim - key0 (this row's last visible column of the
+          // tile) are masked.  L never decreases with the row, so the warp's
+          // first row bounds it below: a 32-column quarter every row of the
+          // warp sees in full (a warp-uniform test) needs no compares.
           const int lim = p.causal ? min(S_kv - 1, i + diag) : S_kv - 1;
+          const int L = lim - key0;
+          const int row_w = row0 + wl * 32;  // the warp's first row
+          const int l_lo = (p.causal ? min(S_kv - 1, row_w + diag) : S_kv - 1) - key0;
 #pragma unroll
-          for (int cc = 0; cc < kBN; ++cc)
-            if (key0 + cc > lim) s[cc] = -INFINITY;
+          for (int qq = 0; qq < kBN / 32; ++qq) {
+            if (l_lo < 32 * qq + 31) {
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                if (32 * qq + e > L) s[32 * qq + e] = -INFINITY;
+            }
+          }
         }
         // Row max: eight independent chains of 3-input max, then a short tree.
         float mx[8];
