@@ -13,22 +13,25 @@
 // Two tensor-core kernels, each with one 128-row tile per CTA:
 //  * dK/dV: a CTA owns 128 keys (K, V resident in shared memory) and walks the
 //    query tiles that see them.  Per tile: S^T = K Q^T and dP^T = V dO^T into
-//    tensor memory; one thread per key row turns them into P^T and dS^T in
-//    place (16-bit pairs over the first half of each); dV += P^T dO and
-//    dK += dS^T Q read P^T / dS^T straight from tensor memory.  Tensor memory:
+//    tensor memory, signalled apart; one thread per key row turns S^T into P^T
+//    first and dP^T into dS^T after (16-bit pairs over each element-wise
+//    group's own columns); dV += P^T dO and dK += dS^T Q read P^T / dS^T
+//    straight from tensor memory, and the next step's S^T follows dV, so dK
+//    and the next dP^T run while the next P^T is computed.  Tensor memory:
 //    S^T [0,128), dP^T [128,256), dV [256,384), dK [384,512).
 //  * dQ: a CTA owns 128 queries (Q, dO resident) and walks the key tiles they
 //    see: S = Q K^T, dP = dO V^T, dS, dQ += dS K.  Tensor memory: S [0,128),
 //    dP [128,256), dQ [256,384), dS [384,448).  Pipelined: once the
 //    element-wise warps hold a step's S and dP in registers, the next step's
 //    products overwrite them while dS is computed; K and V stream through
-//    rings of their own (3 and 2 stages).
+//    rings of their own (3 and 2 stages); one thread issues S and dP, another
+//    dQ += dS K.
 // The dQ pass recomputes S and dP (7 MMAs per tile pair instead of 5) so that
 // no tile's gradient needs atomic accumulation: results are deterministic.
 // A TMA warp streams the walking tiles (dK/dV: a 2-stage ring of (Q, dO)
-// pairs), an MMA warp issues tcgen05.mma, eight warps do the element-wise
-// work (two warpgroups, each taking 64 of the 128 columns of every row);
-// every wait is bounded in time.
+// pairs), MMA-issuing threads in warps 9 (and 10) issue tcgen05.mma, eight
+// warps do the element-wise work (two warpgroups, each taking 64 of the 128
+// columns of every row); every wait is bounded in time.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
